@@ -1,0 +1,484 @@
+"""Benchmark of the tile stitch (and, alongside, every other kernel) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one tb_stitch2d call over the 2048x2048 bf16 workload: batch 4,
+3 channels, a 6x6 grid of 512 px decoded tiles (latent tile 64, overlap 0.25,
+scale 8; blend 128, row_limit 384, last tiles 128 px), synthetic smooth-field
+tiles already resident in HBM.  The metric is GB/s moved (algorithmic bytes:
+every tile element read once plus the output written once, 274.07 MB per
+step), with % of the measured HBM peak and output Mpixel/s.  Three input /
+output sets rotate between steps (822 MB, far above the 129 MB L2), so no
+step finds its inputs in L2.
+
+The JSON line also carries:
+  e2e         the same metric through the C ABI with host buffers: every
+              step copies the tiles from pinned host memory, stitches, and
+              copies the image back;
+  roofline    achieved vs measured HBM bandwidth for the stitch kernel, with
+              the DRAM traffic of the last ncu capture of the same kernel
+              source (null if the source changed since);
+  kernels     every other kernel on its own workload (L2 flushed between
+              launches, CUDA events around each launch);
+  cpu_baseline  the CPU oracle timed on this host on one full step.
+
+Under torchrun (N > 1) every rank runs the same step on its own GPU (weak
+scaling, no collective on the data path); the time is the max over ranks.
+
+--impl reference times the CPU oracle (the unoptimised restatement of the
+method) on bounded samples of the same workload: the only other
+implementation of this path available here.
+"""
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "stitch GB/s moved and % of GB300 HBM peak; output Mpixel/s (2048² bf16 grid)"
+WORKLOAD = "image_2048_bf16"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def stitch_bytes(layouts, planes, esize):
+    """Algorithmic bytes of one stitch: each tile element that is kept or lent
+    to a neighbour's band, read once, plus the output written once."""
+    reads = []
+    for lay in layouts:
+        r = []
+        for n in range(lay.n):
+            e_next = lay.blends[n + 1] if n + 1 < lay.n else 0
+            r.append(min(lay.extents[n], lay.kept[n] + e_next))
+        reads.append(r)
+    tile_elems = 0
+    if len(layouts) == 2:
+        for ry in reads[0]:
+            for rx in reads[1]:
+                tile_elems += ry * rx
+    else:
+        for rt in reads[0]:
+            for ry in reads[1]:
+                for rx in reads[2]:
+                    tile_elems += rt * ry * rx
+    out_elems = 1
+    for lay in layouts:
+        out_elems *= lay.out_extent
+    return planes * (tile_elems + out_elems) * esize, planes * tile_elems * esize, planes * out_elems * esize
+
+
+def source_digest(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key, src_path):
+    """DRAM bytes per launch recorded by the last ncu capture of this kernel,
+    if that capture was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))[kernel_key]
+    except Exception:
+        return None, None
+    if d.get("source_sha256_16") != source_digest(src_path):
+        return None, d.get("capture")
+    return d.get("dram_bytes_per_launch"), d.get("capture")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        self.lines = []
+        try:
+            args = ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits", "-lms", "100"]
+            if gpu_id is not None:
+                args += ["-i", str(gpu_id)]
+            self.proc = subprocess.Popen(args, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S")) + \
+                    (float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0)
+                rows.append(dict(t=ts, sm=float(f[1]), sm_max=float(f[2]), hw=f[5], hw_thermal=f[6],
+                                 sw_thermal=f[7], sw_power=f[8]))
+            except Exception:
+                continue
+        return rows
+
+    @staticmethod
+    def summarise(rows, t0, t1):
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05]
+        window = "timed region"
+        if not inside:
+            # the region was shorter than the sampling period: nearest samples
+            mid = 0.5 * (t0 + t1)
+            inside = sorted(rows, key=lambda r: abs(r["t"] - mid))[:3]
+            window = "nearest samples (timed region %.3f s)" % (t1 - t0)
+        reasons = set()
+        for r in inside:
+            for k, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                            ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside), "sm_max_mhz": max(r["sm_max"] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from patch_groupnorm_gb300 import build as lib_build
+    lib_build.build()
+    from patch_groupnorm_gb300 import tileblend as tb
+    from patch_groupnorm_gb300 import workloads as W
+
+    w = W.STITCH[args.workload]
+    axes = [tb.Axis(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in w.axes]
+    lays = [tb.tb_axis_layout(a) for a in axes]
+    boxes = [list(zip(l.origins, l.extents)) for l in lays]
+    out_ext = [l.out_extent for l in lays]
+    tiles_cpu = W.make_stitch_tiles(w, boxes, out_ext)
+    esize = 4 if w.dtype == "f32" else 2
+    alg_bytes, tile_bytes, out_bytes = stitch_bytes(lays, w.B * w.C, esize)
+    out_shape = (w.B, w.C, *out_ext)
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+
+    nsets = 3
+    sets = []
+    for s in range(nsets):
+        dev_tiles = [[t.to(dev) for t in row] for row in tiles_cpu]
+        out = torch.empty(out_shape, dtype=tdt, device=dev)
+        sets.append((dev_tiles, out))
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    a_y, a_x = axes[0].c(), axes[1].c()
+    code = {"f32": tb.TB_F32, "f16": tb.TB_F16, "bf16": tb.TB_BF16}[w.dtype]
+    calls = []
+    for dev_tiles, out in sets:
+        arr = (ctypes.c_void_p * (lays[0].n * lays[1].n))(*[t.data_ptr() for row in dev_tiles for t in row])
+        calls.append((arr, out.data_ptr()))
+    fn = tb._lib.tb_stitch2d
+    H, Wd = out_ext
+
+    def step(i):
+        arr, optr = calls[i % nsets]
+        st = fn(arr, code, w.B, w.C, ctypes.byref(a_y), ctypes.byref(a_x), optr, H, Wd, sh)
+        if st != 0:
+            raise tb.TileBlendError(st, "tb_stitch2d")
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)  # the sampler's first reading
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    e1.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.15)
+    rows = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        m = torch.tensor([ms], device=dev)
+        dist.all_reduce(m, op=dist.ReduceOp.MAX)
+        ms = float(m.item())
+    ms_per_step = ms / args.steps
+    gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    value = gbs * world
+    peak, peak_kind = measured_peaks()
+    mpix = w.B * H * Wd / (ms_per_step * 1e-3) / 1e6 * world
+    clocks = ClockSampler.summarise(rows, t_wall0, t_wall1)
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_tiles = [[t.pin_memory() for t in row] for row in tiles_cpu]
+        host_out = torch.empty(out_shape, dtype=tdt).pin_memory()
+        dev_tiles, out = sets[0]
+        arr, optr = calls[0]
+        k_e2e = max(3, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            for rh, rd in zip(host_tiles, dev_tiles):
+                for th, td in zip(rh, rd):
+                    td.copy_(th, non_blocking=True)
+            st = fn(arr, code, w.B, w.C, ctypes.byref(a_y), ctypes.byref(a_x), optr, H, Wd, sh)
+            if st != 0:
+                raise tb.TileBlendError(st, "tb_stitch2d")
+            host_out.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        f1.record(stream)
+        f1.synchronize()
+        ems = f0.elapsed_time(f1)
+        if world > 1:
+            m = torch.tensor([ems], device=dev)
+            dist.all_reduce(m, op=dist.ReduceOp.MAX)
+            ems = float(m.item())
+        e2e = {"value": round(alg_bytes / (ems / k_e2e * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": tile_bytes, "d2h_bytes_per_step": out_bytes, "steps": k_e2e,
+               "ms_per_step": round(ems / k_e2e, 4)}
+        # keep the pinned buffers alive until here
+        del host_tiles, host_out
+
+    traffic, capture = profiled_traffic("stitch2d/" + args.workload,
+                                        os.path.join(ROOT, "patch_groupnorm_gb300", "csrc", "tb_stitch.cu"))
+    roofline = {"kernel": "tb::stitch_kernel<2D,bf16>", "bound": "hbm", "achieved": round(gbs, 1),
+                "peak": peak, "peak_kind": "%s (%s)" % (peak_kind, "burst copy, kernel timed alone"),
+                "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": traffic,
+                "traffic_capture": capture, "algorithmic_bytes": alg_bytes}
+
+    kernels = None
+    if not args.no_kernels and rank == 0:
+        kernels = per_kernel(torch, tb, W, dev, peak, args.kernel_reps)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w, lays, tiles_cpu, alg_bytes)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "pct_of_hbm_peak": round(100 * gbs / peak, 2), "mpixel_per_s": round(mpix, 1),
+            "config": {"workload": args.workload, "B": w.B, "C": w.C, "out_hw": out_ext,
+                       "grid": [lays[0].n, lays[1].n], "latent_tile": 64, "overlap": 0.25, "scale": 8,
+                       "algorithmic_bytes_per_step": alg_bytes,
+                       "l2": "3 rotating input/output sets (%.0f MB) > 129 MB L2; no flush" % (
+                           nsets * alg_bytes / 1e6),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps, "roofline": roofline,
+            "cpu_baseline": cpu, "kernels": kernels,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def per_kernel(torch, tb, W, dev, peak, reps):
+    """Every kernel on its own workload: L2 flushed before each launch, CUDA
+    events around the launch; median over reps."""
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = []
+
+    def timed(launch, nbytes, name, workload):
+        ts = []
+        for r in range(reps + 3):
+            flush.fill_(float(r))
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch()
+            b.record(stream)
+            b.synchronize()
+            if r >= 3:
+                ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res.append({"kernel": name, "workload": workload, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                    "frac_of_peak": round(gbs / peak, 4), "bytes": nbytes})
+
+    for name, w in W.STITCH.items():
+        axes = [tb.Axis(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in w.axes]
+        lays = [tb.tb_axis_layout(a) for a in axes]
+        tiles = W.make_stitch_tiles(w, [list(zip(l.origins, l.extents)) for l in lays], [l.out_extent for l in lays])
+        esize = 4 if w.dtype == "f32" else 2
+        nbytes, _, _ = stitch_bytes(lays, w.B * w.C, esize)
+        tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+        if w.ndim == 2:
+            dt = [[t.to(dev) for t in row] for row in tiles]
+            out = torch.empty((w.B, w.C, lays[0].out_extent, lays[1].out_extent), dtype=tdt, device=dev)
+            timed(lambda: tb.tb_stitch2d(dt, axes[0], axes[1], out), nbytes, "stitch2d", name)
+        else:
+            dt = [[[t.to(dev) for t in row] for row in pl] for pl in tiles]
+            out = torch.empty((w.B, w.C, *[l.out_extent for l in lays]), dtype=tdt, device=dev)
+            timed(lambda: tb.tb_stitch3d(dt, axes[0], axes[1], axes[2], out), nbytes, "stitch3d", name)
+        del dt, out
+    for name, w in W.GROUPNORM.items():
+        patches, gamma, beta = W.make_groupnorm_inputs(w)
+        dp = [p.to(dev) for p in patches]
+        g, b = gamma.to(dev), beta.to(dev)
+        outs = [torch.empty_like(p) for p in dp]
+        part = tb.new_partials(len(dp), dp[0].shape[0], w.groups, dev)
+        elems = sum(p.numel() for p in dp)
+        es = dp[0].element_size()
+        timed(lambda: tb.tb_patch_gn_stats(dp, w.groups, part), elems * es, "gn_stats", name)
+        timed(lambda: tb.tb_patch_gn_apply(dp, outs, w.groups, part, g, b, w.eps, True), 2 * elems * es,
+              "gn_apply", name)
+        del dp, outs
+    return res
+
+
+def cpu_baseline(w, lays_lib, tiles_cpu, alg_bytes):
+    """The CPU oracle, as it stands, on one full step of the workload."""
+    import numpy as np
+    import torch
+    from oracle.geometry import axis_layout
+    from oracle.stitch import stitch as oracle_stitch
+
+    lays = [axis_layout(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in w.axes]
+    st = [[t.view(torch.int16).numpy().view(np.uint16) if w.dtype != "f32" else t.numpy() for t in row]
+          for row in tiles_cpu]
+    t0 = time.perf_counter()
+    oracle_stitch(st, lays, w.dtype)
+    dt = time.perf_counter() - t0
+    return {"value": round(alg_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": "one full step (%s: %d tiles, %.1f MB algorithmic), single-threaded C oracle" % (
+                w.name, len(st) * len(st[0]), alg_bytes / 1e6)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle on bounded samples
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    from oracle.geometry import axis_layout
+    from oracle.stitch import stitch as oracle_stitch
+    from patch_groupnorm_gb300 import workloads as W
+
+    w = W.STITCH[args.workload]
+    lays = [axis_layout(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in w.axes]
+    boxes = [[(o * a.scale, L) for o, L in zip(l.origins, l.extents)] for l, a in zip(lays, w.axes)]
+    tiles = W.make_stitch_tiles(w, boxes, [l.out_extent for l in lays])
+    # one (batch, channel) plane per step: 1/12 of the workload
+    st = [[(t[:1, :1].contiguous().view(torch.int16).numpy().view(np.uint16) if w.dtype != "f32"
+            else t[:1, :1].contiguous().numpy()) for t in row] for row in tiles]
+    esize = 4 if w.dtype == "f32" else 2
+    nbytes, _, _ = stitch_bytes(lays, 1, esize)
+    for _ in range(args.warmup):
+        oracle_stitch(st, lays, w.dtype)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_stitch(st, lays, w.dtype)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "config": {"workload": args.workload, "sample": "one (batch, channel) plane"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "per step one (batch, channel) plane of %s (%.1f MB algorithmic)" % (
+                                 w.name, nbytes / 1e6)},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--kernel-reps", type=int, default=30)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kernels", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        if "--steps" not in sys.argv:
+            args.steps = 5
+        if "--warmup" not in sys.argv:
+            args.warmup = 1
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * tileblend.h -- C ABI of libtileblend: tiled-VAE tile stitching and
+ * patch-parallel GroupNorm on NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (web pages, cited by title and section):
+ *   [VTB] "[Proposal] Vectorize tiled VAE blending while preserving rounding
+ *         and CUDA graph replay" (diffusers issue #14722), "Proposed scope".
+ *   [STU] "Studio: size seam-free VAE tiles from measured peaks" (unsloth PR
+ *         #12764), commit "Decode this VAE in 32-latent tiles ...".
+ *   [DVA] "Add tiled VAE parallelism & extended model support" (xDiT
+ *         DistVAE PR #14), the PatchGroupNorm commits.
+ *
+ * Conventions shared by every call
+ *   - Plain C types only.  Device pointers point to memory the caller
+ *     allocated on the current CUDA device; host pointers (pointer tables,
+ *     size arrays, geometry structs) are read before the call returns and may
+ *     be freed right after it.
+ *   - The library allocates no device, pinned or managed memory: all of it
+ *     is the caller's.  Its only state is a small host-side cache of device
+ *     facts (SM count, kernel occupancy) filled on first use per device.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream) and runs asynchronously; a TB_OK return
+ *     means the launch was accepted, not that the kernel finished.  Errors
+ *     raised later by the kernel surface on the caller's next synchronising
+ *     CUDA call.
+ *   - Every argument is validated on the host before anything is launched;
+ *     an invalid call returns an error status and launches nothing.  No call
+ *     aborts, throws or prints.
+ *   - Tensors are dense, contiguous, row-major (last dimension fastest).
+ *   - Kernel parameters are passed by value, so a call can be captured into
+ *     a CUDA graph and replayed with new tensor contents at the same
+ *     addresses.
+ */
+#ifndef TILEBLEND_H
+#define TILEBLEND_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TB_OK = 0,
+    TB_ERR_NULL = 1,        /* a required pointer is NULL */
+    TB_ERR_DTYPE = 2,       /* unknown dtype */
+    TB_ERR_SHAPE = 3,       /* sizes inconsistent with each other or the geometry */
+    TB_ERR_GEOMETRY = 4,    /* tb_axis parameters out of range */
+    TB_ERR_UNSUPPORTED = 5, /* valid request outside what the kernels handle (see each call) */
+    TB_ERR_CUDA = 6         /* the CUDA runtime refused the launch; see tb_last_cuda_error() */
+} tb_status;
+
+typedef enum {
+    TB_F32 = 0,  /* IEEE binary32 */
+    TB_F16 = 1,  /* IEEE binary16 */
+    TB_BF16 = 2  /* bfloat16 (upper half of binary32) */
+} tb_dtype;
+
+/*
+ * One axis of a tile grid, in the parameters the pages use [VTB], [STU]:
+ *   latent_extent  extent of the latent along this axis (latents; frames for
+ *                  a temporal axis given with scale 1)
+ *   latent_tile    tile size in latents
+ *   overlap        overlap factor in [0, 1)
+ *   scale          decoded samples per latent along this axis (>= 1)
+ *   blend_extent   samples cross-faded between neighbours; < 0 derives the
+ *                  stock value int(latent_tile * scale * overlap)
+ *   row_limit      samples each tile keeps; <= 0 derives the stock value
+ *                  latent_tile * scale - blend_extent
+ * Derived grid (the stock tiled decode): stride = int(latent_tile *
+ * (1 - overlap)); tile origins range(0, latent_extent, stride); tile n has
+ * extent L(n) = min(latent_tile, latent_extent - origin) * scale samples;
+ * the blend between tiles n-1 and n is clamped to e(n) = min(L(n-1), L(n),
+ * blend_extent); tile n keeps K(n) = min(L(n), row_limit) samples and the
+ * output extent is the sum of K(n).
+ */
+typedef struct {
+    int32_t latent_extent;
+    int32_t latent_tile;
+    double overlap;
+    int32_t scale;
+    int32_t blend_extent;
+    int32_t row_limit;
+} tb_axis;
+
+/*
+ * Per-patch GroupNorm statistics of one (patch, sample, group) [DVA]:
+ * element count, the patch's own group mean, and the sum of squared
+ * deviations about that mean.  16 bytes, no padding.
+ */
+typedef struct {
+    int64_t n;
+    float mean;
+    float m2;
+} tb_gn_partial;
+
+/* Largest tile count per axis, and per grid, the stitch calls accept. */
+#define TB_MAX_TILES_PER_AXIS 64
+#define TB_MAX_TILES 1024
+
+/* Library version as 10000 * major + 100 * minor + patch. */
+size_t tb_version(void);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* tb_status_string(tb_status status);
+
+/* The cudaError_t value behind the last TB_ERR_CUDA returned on the calling
+ * thread (0 if none). */
+int tb_last_cuda_error(void);
+
+/*
+ * tb_axis_layout -- the derived geometry of one axis (host only, no GPU).
+ *   a            axis parameters (see tb_axis)
+ *   cap          capacity of each output array
+ *   n_tiles      out: number of tiles along the axis
+ *   origins      out, may be NULL: tile n's origin in decoded samples,
+ *                n * stride * scale, for n < min(n_tiles, cap)
+ *   extents      out, may be NULL: L(n) for n < min(n_tiles, cap)
+ *   blends       out, may be NULL: e(n), with e(0) = 0
+ *   kept         out, may be NULL: K(n)
+ *   out_extent   out, may be NULL: sum of K(n)
+ * Returns TB_ERR_GEOMETRY for latent_extent < 0, latent_tile < 1, scale < 1,
+ * an overlap outside [0, 1) or one that leaves a zero stride, or a derived
+ * row_limit < 1; TB_ERR_UNSUPPORTED if the axis has more than
+ * TB_MAX_TILES_PER_AXIS tiles (n_tiles is still written).
+ */
+tb_status tb_axis_layout(const tb_axis* a, int32_t cap, int32_t* n_tiles, int64_t* origins, int32_t* extents,
+                         int32_t* blends, int32_t* kept, int64_t* out_extent);
+
+/*
+ * tb_stitch2d -- stitch a 2D grid of decoded tiles into one image [VTB]:
+ * the result of visiting the tiles in row-major order, cross-fading each
+ * tile's first e_y(i) rows with the already-blended tile above (blend_v),
+ * then its first e_x(j) columns with the already-blended tile to its left
+ * (blend_h), in place, each blend
+ *     b[c] = rnd(rnd(a[L_a - e + c] * (float)(1 - c/e)) + rnd(b[c] * (float)(c/e)))
+ * with the quotients taken in double, the products and the sum in fp32 and
+ * rnd() round-to-nearest-even into the storage dtype; then cropping every
+ * tile to K_y(i) x K_x(j) and concatenating.  The output equals that
+ * sequence bit for bit.  Each output element is computed in one pass from
+ * at most 4 tiles (the closed form of the recurrence).
+ *
+ *   tiles     host array of n_y * n_x device pointers, row-major (i, j);
+ *             tile (i, j) is [B, C, L_y(i), L_x(j)] of `dtype`.  Read only:
+ *             unlike the pages' loops, tiles are NOT modified.
+ *   dtype     storage type of tiles and output
+ *   B, C      batch and channels (>= 0; 0 launches nothing)
+ *   ay, ax    height and width axes of the grid
+ *   out       device pointer, [B, C, out_h, out_w]; must not overlap a tile
+ *   out_h/w   must equal the sum of kept extents of ay / ax
+ * Errors: TB_ERR_NULL (tiles, a tile, out, ay or ax NULL with work to do),
+ * TB_ERR_SHAPE (out_h/out_w mismatch, negative sizes), TB_ERR_GEOMETRY,
+ * TB_ERR_UNSUPPORTED (more than TB_MAX_TILES tiles, or blend bands that
+ * reach each other: every middle tile n must have L(n) >= e(n) + e(n+1) --
+ * true of whole middle tiles whenever overlap <= 1/2), TB_ERR_CUDA.
+ */
+tb_status tb_stitch2d(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C, const tb_axis* ay,
+                      const tb_axis* ax, void* out, int64_t out_h, int64_t out_w, void* stream);
+
+/*
+ * tb_stitch3d -- stitch a 3D grid of decoded video tiles [VTB]: as
+ * tb_stitch2d with a leading frame axis; tiles are visited in row-major
+ * order over (k, i, j) and each tile is blended along time (blend_t, against
+ * the already-blended tile k-1), then height (blend_v), then width
+ * (blend_h); crop to K_t x K_y x K_x and concatenate.  Each output element
+ * is computed from at most 8 tiles.
+ *
+ *   tiles     host array of n_t * n_y * n_x device pointers, row-major
+ *             (k, i, j); tile (k, i, j) is [B, C, L_t(k), L_y(i), L_x(j)]
+ *   at        frame axis (typically scale 1: latent_extent in frames)
+ *   out       [B, C, out_t, out_h, out_w]
+ * Errors as tb_stitch2d.
+ */
+tb_status tb_stitch3d(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C, const tb_axis* at,
+                      const tb_axis* ay, const tb_axis* ax, void* out, int64_t out_t, int64_t out_h,
+                      int64_t out_w, void* stream);
+
+/*
+ * tb_patch_gn_stats -- per-patch GroupNorm partial statistics [DVA].
+ * An activation [N, C, *spatial] is split along one spatial axis into P
+ * patches (the ranks' shards in the pages' patch-parallel decode); patch p is
+ * [N, C, *spatial_p], contiguous, with spatial[p] elements per channel.
+ * Channel c belongs to group c / (C / G).  For every (p, n, g) this writes
+ *   partials[(p * N + n) * G + g] = { count, mean, sum (x - mean)^2 }
+ * over the C/G channels of group g in sample n of patch p (fp32
+ * accumulation, deterministic order).
+ *
+ *   patches   host array of P device pointers
+ *   P         number of patches (1 = plain, unsharded GroupNorm)
+ *   dtype     element type of the patches
+ *   N, C      samples and channels; C % G == 0
+ *   spatial   host array of P element counts per channel (>= 0)
+ *   G         number of groups (>= 1)
+ *   partials  device array of P * N * G tb_gn_partial, written fully
+ * Errors: TB_ERR_NULL, TB_ERR_SHAPE (C % G != 0, negative sizes, P < 1),
+ * TB_ERR_UNSUPPORTED (P > 64), TB_ERR_CUDA.
+ */
+tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dtype dtype, int64_t N, int64_t C,
+                            const int64_t* spatial, int32_t G, tb_gn_partial* partials, void* stream);
+
+/*
+ * tb_patch_gn_apply -- combine the partials of all P patches into the pooled
+ * group mean and the biased variance about it (divided by the total count,
+ * no Bessel correction) [DVA], then normalise, apply the per-channel affine
+ * and optionally SiLU:
+ *     z = (x - mean) / sqrt(var + eps) * gamma[c] + beta[c]
+ *     y = silu ? z / (1 + exp(-z)) : z,   rounded once into dtype.
+ * The result equals GroupNorm (+ SiLU) of the unsharded tensor.
+ *
+ *   patches   host array of P device pointers (as tb_patch_gn_stats)
+ *   outs      host array of P device pointers, same shapes; outs[p] may
+ *             equal patches[p] (in place), other overlaps are not allowed
+ *   partials  device array written by tb_patch_gn_stats for the same
+ *             patches (P * N * G entries)
+ *   gamma     device [C] of dtype, or NULL for 1
+ *   beta      device [C] of dtype, or NULL for 0
+ *   eps       added to the variance (> 0 recommended; >= 0 required)
+ *   silu      nonzero applies SiLU
+ * Errors as tb_patch_gn_stats, plus TB_ERR_SHAPE for eps < 0 or NaN.
+ */
+tb_status tb_patch_gn_apply(const void* const* patches, void* const* outs, int32_t P, tb_dtype dtype, int64_t N,
+                            int64_t C, const int64_t* spatial, int32_t G, const tb_gn_partial* partials,
+                            const void* gamma, const void* beta, float eps, int32_t silu, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILEBLEND_H */

@@ -60,7 +60,7 @@ def axis_layout(latent_extent: int, latent_tile: int, overlap: float, scale: int
         row_limit = latent_tile * scale - blend_extent
     origins = list(range(0, latent_extent, stride))
     extents = [min(latent_tile, latent_extent - o) * scale for o in origins]
-    blends = [0] + [min(extents[n - 1], extents[n], blend_extent) for n in range(1, len(extents))]
+    blends = [0 if n == 0 else min(extents[n - 1], extents[n], blend_extent) for n in range(len(extents))]
     kept = [min(L, row_limit) for L in extents]
     offsets = []
     acc = 0

@@ -1,0 +1,402 @@
+// tb_groupnorm.cu -- patch-parallel GroupNorm (+ SiLU) kernels for sm_103a.
+//
+// What is computed (page "Add tiled VAE parallelism & extended model
+// support", xDiT DistVAE PR #14, the PatchGroupNorm commits): a GroupNorm
+// over an activation split into P patches must equal GroupNorm of the whole
+// tensor -- the group mean pooled over all patches and the biased variance
+// (divided by the count) about that pooled mean -- followed by the affine
+// and, in the decoder blocks, SiLU.
+//
+// The page's implementation meets across ranks twice per norm (one
+// all_reduce for the count and the sums, a second for the squares about the
+// pooled mean, because folding the second into the first would change the
+// estimator).  Here every patch is resident on one GPU, and each patch's
+// statistics travel as (count, mean, M2) -- the sum of squared deviations
+// about the patch's own mean.  Chan's pairwise update combines such triples
+// exactly (up to rounding) into the pooled mean and the M2 about it, so one
+// pass over the data suffices and the combination needs no second reduction:
+//     n = nA + nB,  d = meanB - meanA,
+//     mean = meanA + d * nB / n,  M2 = M2A + M2B + d^2 * nA * nB / n.
+//
+// gn_stats_kernel: one thread-block cluster per (patch, sample, group).  Each
+// thread runs Welford over blocks of 16 elements (block mean and M2 computed
+// directly, then merged), warps merge with shuffles, warps within a CTA
+// through shared memory, and the CTAs of the cluster through distributed
+// shared memory, in a fixed order (deterministic results).  Reads are 128-bit
+// streaming loads.
+//
+// gn_apply_kernel: one CTA per segment of one channel row.  Every warp
+// combines the P partials of its group (lane q holds patch q), forms
+// a = rstd * gamma[c] and b = beta[c] - mean * a, and the elements become
+// y = silu(x * a + b), rounded once into the storage type.
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tb_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace tb {
+namespace {
+
+constexpr int STATS_BLOCK = 256;
+constexpr int APPLY_BLOCK = 128;
+constexpr int APPLY_CPT = 4;  // 16-byte chunks per thread per segment
+
+template <int DT>
+struct GElt;
+template <>
+struct GElt<F32> {
+    static constexpr int BYTES = 4;
+    __device__ __forceinline__ static float to_f(uint32_t v) { return __uint_as_float(v); }
+};
+template <>
+struct GElt<F16> {
+    static constexpr int BYTES = 2;
+    __device__ __forceinline__ static void unpack(uint32_t v, float& lo, float& hi) {
+        float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+        lo = f.x;
+        hi = f.y;
+    }
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    __device__ __forceinline__ static float to_f(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)v)); }
+};
+template <>
+struct GElt<BF16> {
+    static constexpr int BYTES = 2;
+    __device__ __forceinline__ static void unpack(uint32_t v, float& lo, float& hi) {
+        lo = __uint_as_float(v << 16);
+        hi = __uint_as_float(v & 0xffff0000u);
+    }
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    __device__ __forceinline__ static float to_f(uint32_t v) { return __uint_as_float(v << 16); }
+};
+
+// Elements of one 16-byte chunk as floats.
+template <int DT>
+__device__ __forceinline__ void chunk_to_floats(const uint4& v, float (&x)[16 / GElt<DT>::BYTES]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (GElt<DT>::BYTES == 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[q] = __uint_as_float(w[q]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) GElt<DT>::unpack(w[q], x[2 * q], x[2 * q + 1]);
+    }
+}
+
+// Scalar element load (unaligned paths).
+template <int DT>
+__device__ __forceinline__ float load_scalar(const void* base, int64_t i) {
+    if constexpr (GElt<DT>::BYTES == 4) {
+        return __ldcs(reinterpret_cast<const float*>(base) + i);
+    } else {
+        return GElt<DT>::to_f(__ldcs(reinterpret_cast<const unsigned short*>(base) + i));
+    }
+}
+
+struct Stat {
+    float n, mean, m2;
+};
+
+// Chan's pairwise combination of two (count, mean, M2) triples.
+__device__ __forceinline__ Stat chan(const Stat& a, const Stat& b) {
+    if (b.n == 0.f) return a;
+    if (a.n == 0.f) return b;
+    const float n = a.n + b.n;
+    const float r = b.n / n;
+    const float d = b.mean - a.mean;
+    Stat s;
+    s.n = n;
+    s.mean = fmaf(d, r, a.mean);
+    s.m2 = a.m2 + b.m2 + d * d * a.n * r;
+    return s;
+}
+
+// (count, mean, M2) of a block of K elements, computed directly.
+template <int K>
+__device__ __forceinline__ Stat block_stat(const float (&x)[K]) {
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < K; ++q) s += x[q];
+    const float mean = s * (1.0f / K);
+    float m2 = 0.f;
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+        const float d = x[q] - mean;
+        m2 = fmaf(d, d, m2);
+    }
+    return Stat{(float)K, mean, m2};
+}
+
+__device__ __forceinline__ Stat shfl_down_stat(const Stat& s, int delta) {
+    return Stat{__shfl_down_sync(0xffffffffu, s.n, delta), __shfl_down_sync(0xffffffffu, s.mean, delta),
+                __shfl_down_sync(0xffffffffu, s.m2, delta)};
+}
+
+__device__ __forceinline__ Stat warp_reduce(Stat s) {
+#pragma unroll
+    for (int delta = 16; delta >= 1; delta >>= 1) s = chan(s, shfl_down_stat(s, delta));
+    return s;  // valid in lane 0
+}
+
+template <int DT, bool VECTOR>
+__global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_constant__ GnStatsParams p) {
+    constexpr int VEC = 16 / GElt<DT>::BYTES;
+    __shared__ Stat s_warp[STATS_BLOCK / 32];
+    __shared__ Stat s_cta;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int cs = p.cs;
+    const int64_t unit = blockIdx.x / cs;
+    const int rank = (int)cluster.block_rank();
+    const int64_t NG = p.N * p.G;
+    const int pp = (int)(unit / NG);
+    const int64_t rem = unit - (int64_t)pp * NG;
+    const int64_t n = rem / p.G;
+    const int64_t g = rem - n * p.G;
+    const int64_t S = p.spatial[pp];
+    const int64_t cg_ = p.C / p.G;
+    const int64_t len = cg_ * S;
+    const int64_t start = (n * p.C + g * cg_) * S;
+    const char* base = reinterpret_cast<const char*>(p.patches[pp]) + start * GElt<DT>::BYTES;
+
+    Stat acc{0.f, 0.f, 0.f};
+    if constexpr (VECTOR) {
+        // len and start are multiples of VEC: whole 16-byte chunks
+        const int64_t nv = len / VEC;
+        const int64_t v0 = nv * rank / cs, v1 = nv * (rank + 1) / cs;
+        const uint4* src = reinterpret_cast<const uint4*>(base);
+        int64_t v = v0 + threadIdx.x;
+        // two chunks per step: 2 x 16-byte loads in flight, one 2*VEC-element merge
+        for (; v + STATS_BLOCK < v1; v += 2 * STATS_BLOCK) {
+            const uint4 a = __ldcs(src + v);
+            const uint4 b = __ldcs(src + v + STATS_BLOCK);
+            float x[2 * VEC];
+            float xa[VEC], xb[VEC];
+            chunk_to_floats<DT>(a, xa);
+            chunk_to_floats<DT>(b, xb);
+#pragma unroll
+            for (int q = 0; q < VEC; ++q) {
+                x[q] = xa[q];
+                x[VEC + q] = xb[q];
+            }
+            acc = chan(acc, block_stat<2 * VEC>(x));
+        }
+        if (v < v1) {
+            float x[VEC];
+            chunk_to_floats<DT>(__ldcs(src + v), x);
+            acc = chan(acc, block_stat<VEC>(x));
+        }
+    } else {
+        const int64_t e0 = len * rank / cs, e1 = len * (rank + 1) / cs;
+        for (int64_t e = e0 + threadIdx.x; e < e1; e += STATS_BLOCK) {
+            const float x = load_scalar<DT>(base, e);
+            acc = chan(acc, Stat{1.f, x, 0.f});
+        }
+    }
+
+    // warp, then CTA (fixed order), then cluster (fixed order)
+    acc = warp_reduce(acc);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) s_warp[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Stat t = s_warp[0];
+#pragma unroll
+        for (int w = 1; w < STATS_BLOCK / 32; ++w) t = chan(t, s_warp[w]);
+        s_cta = t;
+    }
+    cluster.sync();
+    if (rank == 0 && threadIdx.x == 0) {
+        Stat t = s_cta;
+        for (int r = 1; r < cs; ++r) t = chan(t, *cluster.map_shared_rank(&s_cta, r));
+        GnPartial out;
+        out.n = len;
+        out.mean = len > 0 ? t.mean : 0.f;
+        out.m2 = len > 0 ? t.m2 : 0.f;
+        p.partials[unit] = out;
+    }
+    cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
+}
+
+// Pooled (mean, rstd) of group g of sample n from the P partials; every
+// lane of the warp returns the same values.
+__device__ __forceinline__ void pooled_stats(const GnApplyParams& p, int64_t n, int64_t g, float& mean, float& rstd) {
+    const int lane = threadIdx.x & 31;
+    Stat s{0.f, 0.f, 0.f};
+    for (int q = lane; q < p.P; q += 32) {
+        const GnPartial* src = p.partials + ((int64_t)q * p.N + n) * p.G + g;
+        const longlong2 raw = __ldg(reinterpret_cast<const longlong2*>(src));
+        const float pm = __int_as_float((int)(raw.y & 0xffffffffLL));
+        const float pm2 = __int_as_float((int)(raw.y >> 32));
+        s = chan(s, Stat{(float)raw.x, pm, pm2});
+    }
+    s = warp_reduce(s);
+    const float tn = __shfl_sync(0xffffffffu, s.n, 0);
+    const float tm = __shfl_sync(0xffffffffu, s.mean, 0);
+    const float tm2 = __shfl_sync(0xffffffffu, s.m2, 0);
+    const float var = tn > 0.f ? tm2 / tn : 0.f;  // biased: divide by the count
+    mean = tm;
+    rstd = 1.0f / sqrtf(var + p.eps);
+}
+
+template <int DT>
+__device__ __forceinline__ float load_param(const void* ptr, int64_t c, float dflt) {
+    if (ptr == nullptr) return dflt;
+    if constexpr (GElt<DT>::BYTES == 4) {
+        return __ldg(reinterpret_cast<const float*>(ptr) + c);
+    } else {
+        return GElt<DT>::to_f(__ldg(reinterpret_cast<const unsigned short*>(ptr) + c));
+    }
+}
+
+template <int SILU>
+__device__ __forceinline__ float act(float x, float a, float b) {
+    const float z = fmaf(x, a, b);
+    if constexpr (SILU) {
+        return __fdividef(z, 1.0f + __expf(-z));
+    } else {
+        return z;
+    }
+}
+
+template <int DT, bool VECTOR, int SILU>
+__global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_constant__ GnApplyParams p) {
+    constexpr int VEC = VECTOR ? 16 / GElt<DT>::BYTES : 1;
+    const int64_t item = blockIdx.x;
+    int pp = 0;
+    while (pp + 1 < p.P && p.item_start[pp + 1] <= item) ++pp;
+    const int64_t local = item - p.item_start[pp];
+    const int64_t nseg = p.nseg[pp];
+    const int64_t row = local / nseg;  // n * C + c
+    const int64_t seg = local - row * nseg;
+    const int64_t S = p.spatial[pp];
+    const int64_t c = row % p.C;
+    const int64_t n = row / p.C;
+    const int64_t g = c / (p.C / p.G);
+    const int64_t e_begin = seg * p.seg;
+    const int64_t e_end = min(S, e_begin + p.seg);
+    const int64_t row_start = row * S;
+
+    if constexpr (VECTOR) {
+        // S and every row start are multiples of VEC; issue the data loads first
+        const uint4* src = reinterpret_cast<const uint4*>(p.patches[pp]) + (row_start + e_begin) / VEC;
+        uint4* dst = reinterpret_cast<uint4*>(p.outs[pp]) + (row_start + e_begin) / VEC;
+        const int nchunk = (int)((e_end - e_begin) / VEC);
+        uint4 v[APPLY_CPT];
+#pragma unroll
+        for (int q = 0; q < APPLY_CPT; ++q) {
+            const int idx = threadIdx.x + q * APPLY_BLOCK;
+            if (idx < nchunk) v[q] = __ldcs(src + idx);
+        }
+        float mean, rstd;
+        pooled_stats(p, n, g, mean, rstd);
+        const float a = rstd * load_param<DT>(p.gamma, c, 1.f);
+        const float b = load_param<DT>(p.beta, c, 0.f) - mean * a;
+#pragma unroll
+        for (int q = 0; q < APPLY_CPT; ++q) {
+            const int idx = threadIdx.x + q * APPLY_BLOCK;
+            if (idx >= nchunk) continue;
+            uint4 o;
+            if constexpr (GElt<DT>::BYTES == 4) {
+                o.x = __float_as_uint(act<SILU>(__uint_as_float(v[q].x), a, b));
+                o.y = __float_as_uint(act<SILU>(__uint_as_float(v[q].y), a, b));
+                o.z = __float_as_uint(act<SILU>(__uint_as_float(v[q].z), a, b));
+                o.w = __float_as_uint(act<SILU>(__uint_as_float(v[q].w), a, b));
+            } else {
+                uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float lo, hi;
+                    GElt<DT>::unpack(w[k], lo, hi);
+                    w[k] = GElt<DT>::pack(act<SILU>(lo, a, b), act<SILU>(hi, a, b));
+                }
+                o = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            __stcs(dst + idx, o);
+        }
+    } else {
+        float mean, rstd;
+        pooled_stats(p, n, g, mean, rstd);
+        const float a = rstd * load_param<DT>(p.gamma, c, 1.f);
+        const float b = load_param<DT>(p.beta, c, 0.f) - mean * a;
+        const void* src = p.patches[pp];
+        void* dst = p.outs[pp];
+        for (int64_t e = e_begin + threadIdx.x; e < e_end; e += APPLY_BLOCK) {
+            const float y = act<SILU>(load_scalar<DT>(src, row_start + e), a, b);
+            if constexpr (GElt<DT>::BYTES == 4) {
+                __stcs(reinterpret_cast<float*>(dst) + row_start + e, y);
+            } else {
+                __stcs(reinterpret_cast<unsigned short*>(dst) + row_start + e,
+                       (unsigned short)(GElt<DT>::pack(y, 0.f) & 0xffffu));
+            }
+        }
+    }
+}
+
+template <int DT>
+cudaError_t stats_dt(const GnStatsParams& p, int64_t units, cudaStream_t s) {
+    void (*fn)(const GnStatsParams) = p.aligned ? gn_stats_kernel<DT, true> : gn_stats_kernel<DT, false>;
+    if (p.cs > 8) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * p.cs), 1, 1);
+    cfg.blockDim = dim3(STATS_BLOCK, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+template <int DT>
+cudaError_t apply_dt(const GnApplyParams& p, int64_t items, cudaStream_t s) {
+    void (*fn)(const GnApplyParams);
+    if (p.aligned) {
+        fn = p.silu ? gn_apply_kernel<DT, true, 1> : gn_apply_kernel<DT, true, 0>;
+    } else {
+        fn = p.silu ? gn_apply_kernel<DT, false, 1> : gn_apply_kernel<DT, false, 0>;
+    }
+    fn<<<(unsigned)items, APPLY_BLOCK, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gn_apply_segment(int dtype, bool aligned) {
+    const int bytes = dtype == F32 ? 4 : 2;
+    return APPLY_BLOCK * (aligned ? APPLY_CPT * (16 / bytes) : APPLY_CPT);
+}
+
+cudaError_t launch_gn_stats(const GnStatsParams& p, int dtype, int64_t units, cudaStream_t s) {
+    switch (dtype) {
+        case F32: return stats_dt<F32>(p, units, s);
+        case F16: return stats_dt<F16>(p, units, s);
+        default: return stats_dt<BF16>(p, units, s);
+    }
+}
+
+cudaError_t launch_gn_apply(const GnApplyParams& p, int dtype, int64_t items, cudaStream_t s) {
+    switch (dtype) {
+        case F32: return apply_dt<F32>(p, items, s);
+        case F16: return apply_dt<F16>(p, items, s);
+        default: return apply_dt<BF16>(p, items, s);
+    }
+}
+
+}  // namespace tb

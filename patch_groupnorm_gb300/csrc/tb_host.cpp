@@ -1,0 +1,466 @@
+// tb_host.cpp -- libtileblend's C ABI: argument validation, tile-grid
+// geometry, blend coefficient tables, launch configuration.
+//
+// Geometry follows the stock tiled decode (page "Studio: size seam-free VAE
+// tiles from measured peaks", commit "Decode this VAE in 32-latent tiles
+// ...": 256 px tiles with a 192 px stride and a 64 px blend at 16x; page
+// "[Proposal] Vectorize tiled VAE blending ...", "Proposed scope": clamped
+// blend extents):
+//     stride = int(latent_tile * (1 - overlap))
+//     origins = range(0, latent_extent, stride)
+//     L(n) = min(latent_tile, latent_extent - origin) * scale
+//     blend_extent = int(latent_tile * scale * overlap),  row_limit = tile - blend_extent
+//     e(n) = min(L(n-1), L(n), blend_extent),  K(n) = min(L(n), row_limit)
+// The blend coefficients are the pages' Python-double quotients c/e and
+// 1 - c/e, narrowed to fp32 ("float64 tensor division to match
+// Python-double rounding", same page), computed here once per distinct e.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "tb_internal.h"
+#include "tileblend.h"
+
+#define TB_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+tb_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return TB_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// geometry
+// ---------------------------------------------------------------------------
+
+struct Axis {
+    int32_t n = 0;
+    int64_t stride = 0;
+    int32_t ext[TB_MAX_TILES_PER_AXIS] = {};
+    int32_t blend[TB_MAX_TILES_PER_AXIS] = {};
+    int32_t kept[TB_MAX_TILES_PER_AXIS] = {};
+    int32_t blend_extent = 0;
+    int32_t row_limit = 0;
+    int64_t out = 0;
+};
+
+// Validates `a` and derives its grid.  *n_total receives the tile count even
+// when it exceeds TB_MAX_TILES_PER_AXIS (then TB_ERR_UNSUPPORTED).
+tb_status derive_axis(const tb_axis* a, Axis& g, int64_t* n_total) {
+    if (a == nullptr) return TB_ERR_NULL;
+    if (a->latent_extent < 0 || a->latent_tile < 1 || a->scale < 1) return TB_ERR_GEOMETRY;
+    if (!(a->overlap >= 0.0 && a->overlap < 1.0)) return TB_ERR_GEOMETRY;
+    const double tile_px = (double)a->latent_tile * (double)a->scale;
+    if (tile_px > 2147483647.0) return TB_ERR_GEOMETRY;
+    const int64_t stride = (int64_t)((double)a->latent_tile * (1.0 - a->overlap));
+    if (stride < 1) return TB_ERR_GEOMETRY;
+    const int64_t be = a->blend_extent < 0 ? (int64_t)((double)((int64_t)a->latent_tile * a->scale) * a->overlap)
+                                           : (int64_t)a->blend_extent;
+    const int64_t rl = a->row_limit <= 0 ? (int64_t)a->latent_tile * a->scale - be : (int64_t)a->row_limit;
+    if (rl < 1 || be > 2147483647LL || rl > 2147483647LL) return TB_ERR_GEOMETRY;
+    const int64_t n = a->latent_extent == 0 ? 0 : ((int64_t)a->latent_extent + stride - 1) / stride;
+    if (n_total) *n_total = n;
+    if (n > TB_MAX_TILES_PER_AXIS) return TB_ERR_UNSUPPORTED;
+    g.n = (int32_t)n;
+    g.stride = stride;
+    g.blend_extent = (int32_t)be;
+    g.row_limit = (int32_t)rl;
+    g.out = 0;
+    for (int64_t k = 0; k < n; ++k) {
+        const int64_t origin = k * stride;
+        const int64_t lat = std::min<int64_t>(a->latent_tile, a->latent_extent - origin);
+        const int64_t L = lat * a->scale;
+        if (L > 2147483647LL) return TB_ERR_GEOMETRY;
+        g.ext[k] = (int32_t)L;
+        g.blend[k] = k == 0 ? 0 : (int32_t)std::min<int64_t>(std::min<int64_t>(g.ext[k - 1], L), be);
+        g.kept[k] = (int32_t)std::min<int64_t>(L, rl);
+        g.out += g.kept[k];
+    }
+    if (g.out > 2147483647LL) return TB_ERR_GEOMETRY;
+    return TB_OK;
+}
+
+// Bands that reach each other (a middle tile's lent rows rewritten by its
+// own band) fall outside the closed form the kernels evaluate.
+bool bands_apart(const Axis& g) {
+    for (int k = 1; k + 1 < g.n; ++k)
+        if ((int64_t)g.ext[k] < (int64_t)g.blend[k] + g.blend[k + 1]) return false;
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// device facts, cached per device (no allocation)
+// ---------------------------------------------------------------------------
+
+constexpr int MAX_DEVICES = 64;
+int g_sm_count[MAX_DEVICES] = {};
+std::mutex g_mu;
+
+tb_status device_sms(int* sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev >= 0 && dev < MAX_DEVICES && g_sm_count[dev] > 0) {
+        *sms = g_sm_count[dev];
+        return TB_OK;
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev >= 0 && dev < MAX_DEVICES) g_sm_count[dev] = n;
+    *sms = n;
+    return TB_OK;
+}
+
+// occupancy per (device, kernel variant, block size), cached
+struct OccKey {
+    int dev, ndim, dtype, vec, kx, block, large;
+};
+constexpr int OCC_CAP = 256;
+OccKey g_occ_key[OCC_CAP];
+int g_occ_val[OCC_CAP];
+int g_occ_n = 0;
+
+int stitch_occupancy(const tb::StitchLaunch& l, bool large) {
+    int dev = 0;
+    (void)cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int q = 0; q < g_occ_n; ++q) {
+        const OccKey& k = g_occ_key[q];
+        if (k.dev == dev && k.ndim == l.ndim && k.dtype == l.dtype && k.vec == l.vec && k.kx == l.kx &&
+            k.block == l.block && k.large == (int)large)
+            return g_occ_val[q];
+    }
+    const int v = tb::stitch_kernel_max_ctas_per_sm(l, large);
+    if (g_occ_n < OCC_CAP) {
+        g_occ_key[g_occ_n] = OccKey{dev, l.ndim, l.dtype, l.vec, l.kx, l.block, (int)large};
+        g_occ_val[g_occ_n] = v;
+        ++g_occ_n;
+    }
+    return v;
+}
+
+int elem_bytes(tb_dtype d) { return d == TB_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// stitch
+// ---------------------------------------------------------------------------
+
+template <class P>
+tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, int64_t planes,
+                          const void* const* tiles, void* out, cudaStream_t stream, bool large) {
+    constexpr int MAXA = sizeof(prm.ax[0].ext) / sizeof(int32_t);
+    constexpr int MAXC = sizeof(prm.coef) / sizeof(float2);
+    std::memset(&prm, 0, sizeof(prm));
+    // coefficient tables, one per distinct clamped blend extent
+    int32_t distinct_e[3 * TB_MAX_TILES_PER_AXIS];
+    int32_t distinct_off[3 * TB_MAX_TILES_PER_AXIS];
+    int nd = 0, ncoef = 0;
+    for (int a = 0; a < 3; ++a) {
+        auto& ax = prm.ax[a];
+        ax.n = g[a].n;
+        int32_t acc = 0;
+        for (int k = 0; k < g[a].n; ++k) {
+            ax.ext[k] = g[a].ext[k];
+            ax.blend[k] = g[a].blend[k];
+            ax.off[k] = acc;
+            acc += g[a].kept[k];
+            const int32_t e = g[a].blend[k];
+            ax.coef[k] = 0;
+            if (e <= 0) continue;
+            int f = 0;
+            while (f < nd && distinct_e[f] != e) ++f;
+            if (f == nd) {
+                if (ncoef + e > MAXC) return TB_ERR_UNSUPPORTED;
+                distinct_e[nd] = e;
+                distinct_off[nd] = ncoef;
+                for (int32_t c = 0; c < e; ++c) {
+                    const double q = (double)c / (double)e;
+                    prm.coef[ncoef + c] = make_float2((float)q, (float)(1.0 - (double)c / (double)e));
+                }
+                ncoef += e;
+                ++nd;
+            }
+            ax.coef[k] = distinct_off[f];
+        }
+        ax.off[g[a].n] = acc;
+    }
+    (void)MAXA;
+    prm.ncoef = ncoef;
+    const int ntiles = g[0].n * g[1].n * g[2].n;
+    for (int q = 0; q < ntiles; ++q) prm.tiles[q] = tiles[q];
+    prm.out = out;
+    prm.planes = planes;
+    prm.OT = (int32_t)g[0].out;
+    prm.OH = (int32_t)g[1].out;
+    prm.OW = (int32_t)g[2].out;
+
+    // 16-byte chunks where the width geometry and every pointer allow it
+    const int eb = elem_bytes(dtype);
+    int vec = 16 / eb;
+    bool ok = (prm.OW % vec == 0) && aligned16(out);
+    for (int k = 0; ok && k < g[2].n; ++k)
+        ok = g[2].ext[k] % vec == 0 && g[2].kept[k] % vec == 0 && g[2].blend[k] % vec == 0;
+    for (int q = 0; ok && q < ntiles; ++q) ok = aligned16(tiles[q]);
+    if (!ok) vec = 1;
+
+    tb::StitchLaunch l{};
+    l.ndim = ndim;
+    l.dtype = (int)dtype;
+    l.vec = vec;
+    l.kx = 1;
+    const int64_t wc = prm.OW / vec;  // chunks per output row
+    int xt, nseg;
+    if (wc <= 512) {
+        xt = (int)wc;
+        nseg = 1;
+    } else {
+        xt = 256;
+        nseg = (int)((wc + xt * l.kx - 1) / (xt * l.kx));
+    }
+    const int rp = xt >= 256 ? 1 : (256 + xt - 1) / xt;
+    prm.xt = xt;
+    prm.rp = rp;
+    prm.nseg = nseg;
+    prm.seg_chunks = xt * l.kx;
+    const int64_t rows = planes * (int64_t)prm.OT * prm.OH;
+    prm.nvrows = rows * nseg;
+    if (prm.nvrows >= (int64_t)1 << 31) return TB_ERR_UNSUPPORTED;
+    l.block = xt * rp;
+
+    int sms = 0;
+    tb_status st = device_sms(&sms);
+    if (st != TB_OK) return st;
+    const int per_sm = stitch_occupancy(l, large);
+    const int64_t want = (prm.nvrows + rp - 1) / rp;
+    const int64_t cap = (int64_t)sms * per_sm;
+    l.grid = (int)(want < cap ? want : cap);
+
+    cudaError_t e;
+    if constexpr (sizeof(P) == sizeof(tb::StitchParamsLarge)) {
+        e = tb::launch_stitch_large(prm, l, stream);
+    } else {
+        e = tb::launch_stitch_small(prm, l, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return TB_OK;
+}
+
+tb_status stitch_common(int ndim, const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
+                        const tb_axis* at, const tb_axis* ay, const tb_axis* ax, void* out, int64_t out_t,
+                        int64_t out_h, int64_t out_w, void* stream) {
+    if (dtype != TB_F32 && dtype != TB_F16 && dtype != TB_BF16) return TB_ERR_DTYPE;
+    if (B < 0 || C < 0 || out_t < 0 || out_h < 0 || out_w < 0) return TB_ERR_SHAPE;
+    Axis g[3];
+    int64_t ntot = 0;
+    if (ndim == 3) {
+        tb_status s = derive_axis(at, g[0], &ntot);
+        if (s != TB_OK) return s;
+    } else {
+        g[0].n = 1;
+        g[0].ext[0] = 1;
+        g[0].kept[0] = 1;
+        g[0].blend[0] = 0;
+        g[0].out = 1;
+    }
+    tb_status s = derive_axis(ay, g[1], &ntot);
+    if (s != TB_OK) return s;
+    s = derive_axis(ax, g[2], &ntot);
+    if (s != TB_OK) return s;
+    if ((ndim == 3 && out_t != g[0].out) || out_h != g[1].out || out_w != g[2].out) return TB_ERR_SHAPE;
+    const int64_t planes = B * C;
+    const int64_t ntiles = (int64_t)g[0].n * g[1].n * g[2].n;
+    if (planes == 0 || ntiles == 0) return TB_OK;  // nothing to write
+    if (B > 0 && planes / B != C) return TB_ERR_SHAPE;
+    if (tiles == nullptr || out == nullptr) return TB_ERR_NULL;
+    if (ntiles > TB_MAX_TILES) return TB_ERR_UNSUPPORTED;
+    for (int64_t q = 0; q < ntiles; ++q)
+        if (tiles[q] == nullptr) return TB_ERR_NULL;
+    for (int a = 0; a < 3; ++a)
+        if (!bands_apart(g[a])) return TB_ERR_UNSUPPORTED;
+    // every tile's element count must fit the kernel's 64-bit offsets (always)
+    // and the output row count its 32-bit row arithmetic (checked at launch)
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool small = g[0].n <= tb::SMALL_MAXA && g[1].n <= tb::SMALL_MAXA && g[2].n <= tb::SMALL_MAXA &&
+                       ntiles <= tb::SMALL_MAXT;
+    if (small) {
+        tb::StitchParamsSmall prm;
+        tb_status r = fill_and_launch(prm, g, ndim, dtype, planes, tiles, out, st, false);
+        if (r != TB_ERR_UNSUPPORTED) return r;
+    }
+    tb::StitchParamsLarge prm_l;
+    return fill_and_launch(prm_l, g, ndim, dtype, planes, tiles, out, st, true);
+}
+
+// ---------------------------------------------------------------------------
+// PatchGroupNorm
+// ---------------------------------------------------------------------------
+
+tb_status gn_validate(const void* const* patches, int32_t P, tb_dtype dtype, int64_t N, int64_t C,
+                      const int64_t* spatial, int32_t G, const void* partials) {
+    if (dtype != TB_F32 && dtype != TB_F16 && dtype != TB_BF16) return TB_ERR_DTYPE;
+    if (P < 1 || N < 0 || C < 0 || G < 1) return TB_ERR_SHAPE;
+    if (C % G != 0) return TB_ERR_SHAPE;
+    if (P > tb::GN_MAXP) return TB_ERR_UNSUPPORTED;
+    if (spatial == nullptr || patches == nullptr) return TB_ERR_NULL;
+    for (int p = 0; p < P; ++p) {
+        if (spatial[p] < 0) return TB_ERR_SHAPE;
+        if (N > 0 && C > 0 && spatial[p] > 0 && patches[p] == nullptr) return TB_ERR_NULL;
+        // element counts must stay well inside int64
+        if (spatial[p] > 0 && N > 0 && C > 0 && (double)N * (double)C * (double)spatial[p] > 9.0e18)
+            return TB_ERR_SHAPE;
+    }
+    if (N > 0 && C > 0 && partials == nullptr) return TB_ERR_NULL;
+    if ((double)P * (double)N * (double)G > 2.0e9) return TB_ERR_UNSUPPORTED;
+    return TB_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+
+TB_API size_t tb_version(void) { return 10000 * 0 + 100 * 1 + 0; }
+
+TB_API const char* tb_status_string(tb_status s) {
+    switch (s) {
+        case TB_OK: return "ok";
+        case TB_ERR_NULL: return "a required pointer is NULL";
+        case TB_ERR_DTYPE: return "unknown dtype";
+        case TB_ERR_SHAPE: return "sizes are inconsistent";
+        case TB_ERR_GEOMETRY: return "tile-grid geometry out of range";
+        case TB_ERR_UNSUPPORTED: return "request outside what the kernels handle";
+        case TB_ERR_CUDA: return "the CUDA runtime refused the launch";
+    }
+    return "unknown status";
+}
+
+TB_API int tb_last_cuda_error(void) { return g_last_cuda_error; }
+
+TB_API tb_status tb_axis_layout(const tb_axis* a, int32_t cap, int32_t* n_tiles, int64_t* origins, int32_t* extents,
+                                int32_t* blends, int32_t* kept, int64_t* out_extent) {
+    if (a == nullptr || n_tiles == nullptr) return TB_ERR_NULL;
+    Axis g;
+    int64_t ntot = 0;
+    tb_status s = derive_axis(a, g, &ntot);
+    if (s == TB_ERR_UNSUPPORTED) {
+        *n_tiles = (int32_t)std::min<int64_t>(ntot, 2147483647LL);
+        return s;
+    }
+    if (s != TB_OK) return s;
+    *n_tiles = g.n;
+    for (int k = 0; k < g.n && k < cap; ++k) {
+        if (origins) origins[k] = (int64_t)k * g.stride * a->scale;
+        if (extents) extents[k] = g.ext[k];
+        if (blends) blends[k] = g.blend[k];
+        if (kept) kept[k] = g.kept[k];
+    }
+    if (out_extent) *out_extent = g.out;
+    return TB_OK;
+}
+
+TB_API tb_status tb_stitch2d(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C, const tb_axis* ay,
+                             const tb_axis* ax, void* out, int64_t out_h, int64_t out_w, void* stream) {
+    return stitch_common(2, tiles, dtype, B, C, nullptr, ay, ax, out, 1, out_h, out_w, stream);
+}
+
+TB_API tb_status tb_stitch3d(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C, const tb_axis* at,
+                             const tb_axis* ay, const tb_axis* ax, void* out, int64_t out_t, int64_t out_h,
+                             int64_t out_w, void* stream) {
+    if (at == nullptr) return TB_ERR_NULL;
+    return stitch_common(3, tiles, dtype, B, C, at, ay, ax, out, out_t, out_h, out_w, stream);
+}
+
+TB_API tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dtype dtype, int64_t N, int64_t C,
+                                   const int64_t* spatial, int32_t G, tb_gn_partial* partials, void* stream) {
+    tb_status s = gn_validate(patches, P, dtype, N, C, spatial, G, partials);
+    if (s != TB_OK) return s;
+    if (N == 0 || C == 0) return TB_OK;
+    tb::GnStatsParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    const int vec = 16 / elem_bytes(dtype);
+    const int64_t cg = C / G;
+    bool aligned = true;
+    int64_t max_len = 0;
+    for (int p = 0; p < P; ++p) {
+        prm.patches[p] = patches[p];
+        prm.spatial[p] = spatial[p];
+        const int64_t len = cg * spatial[p];
+        max_len = std::max(max_len, len);
+        if (spatial[p] > 0 && (!aligned16(patches[p]) || len % vec != 0)) aligned = false;
+    }
+    prm.partials = reinterpret_cast<tb::GnPartial*>(partials);
+    prm.N = N;
+    prm.C = C;
+    prm.P = P;
+    prm.G = G;
+    prm.aligned = aligned ? 1 : 0;
+    // CTAs per unit: enough to fill the GPU about twice, each with >= 32 KB
+    int sms = 0;
+    s = device_sms(&sms);
+    if (s != TB_OK) return s;
+    const int64_t units = (int64_t)P * N * G;
+    const int64_t bytes = max_len * elem_bytes(dtype);
+    int cs = 1;
+    while (cs < 16 && units * cs < 2LL * sms * 4 && bytes / (cs * 2) >= 32768) cs *= 2;
+    prm.cs = cs;
+    if (units * cs > 2147483647LL) return TB_ERR_UNSUPPORTED;
+    cudaError_t e = tb::launch_gn_stats(prm, (int)dtype, units, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return TB_OK;
+}
+
+TB_API tb_status tb_patch_gn_apply(const void* const* patches, void* const* outs, int32_t P, tb_dtype dtype, int64_t N,
+                                   int64_t C, const int64_t* spatial, int32_t G, const tb_gn_partial* partials,
+                                   const void* gamma, const void* beta, float eps, int32_t silu, void* stream) {
+    tb_status s = gn_validate(patches, P, dtype, N, C, spatial, G, partials);
+    if (s != TB_OK) return s;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return TB_ERR_SHAPE;
+    if (outs == nullptr) return TB_ERR_NULL;
+    if (N == 0 || C == 0) return TB_OK;
+    for (int p = 0; p < P; ++p)
+        if (spatial[p] > 0 && outs[p] == nullptr) return TB_ERR_NULL;
+    tb::GnApplyParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    const int vec = 16 / elem_bytes(dtype);
+    bool aligned = true;
+    for (int p = 0; p < P; ++p) {
+        if (spatial[p] > 0 && (spatial[p] % vec != 0 || !aligned16(patches[p]) || !aligned16(outs[p])))
+            aligned = false;
+    }
+    const int64_t seg = tb::gn_apply_segment((int)dtype, aligned);
+    int64_t items = 0;
+    for (int p = 0; p < P; ++p) {
+        prm.patches[p] = patches[p];
+        prm.outs[p] = outs[p];
+        prm.spatial[p] = spatial[p];
+        prm.item_start[p] = items;
+        prm.nseg[p] = spatial[p] > 0 ? (spatial[p] + seg - 1) / seg : 1;
+        if (spatial[p] > 0) items += N * C * prm.nseg[p];
+    }
+    prm.item_start[P] = items;  // a patch with no elements owns an empty item range
+    if (items == 0) return TB_OK;
+    if (items > 2147483647LL) return TB_ERR_UNSUPPORTED;
+    prm.partials = reinterpret_cast<const tb::GnPartial*>(partials);
+    prm.gamma = gamma;
+    prm.beta = beta;
+    prm.N = N;
+    prm.C = C;
+    prm.P = P;
+    prm.G = G;
+    prm.seg = (int32_t)seg;
+    prm.eps = eps;
+    prm.silu = silu ? 1 : 0;
+    prm.aligned = aligned ? 1 : 0;
+    cudaError_t e = tb::launch_gn_apply(prm, (int)dtype, items, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return TB_OK;
+}

@@ -1,0 +1,314 @@
+"""Python binding of libtileblend (include/tileblend.h).
+
+Argument marshalling only: every step of the stitch and of PatchGroupNorm
+runs in the library's CUDA kernels.  Tensors must be CUDA tensors on the
+current device, contiguous, of one dtype (float32, float16 or bfloat16).
+Calls are asynchronous on the current torch stream unless ``stream`` (a
+``torch.cuda.Stream`` or a raw ``cudaStream_t`` integer) is given.
+
+There is no fallback: if the compiled library is missing, importing this
+module raises.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libtileblend.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libtileblend.so is not built (expected at %s); run "
+        "`python -c 'import __graft_entry__ as g; g.build()'` or "
+        "`python patch_groupnorm_gb300/build.py`" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---------------------------------------------------------------------------
+# C declarations
+# ---------------------------------------------------------------------------
+
+TB_OK, TB_ERR_NULL, TB_ERR_DTYPE, TB_ERR_SHAPE, TB_ERR_GEOMETRY, TB_ERR_UNSUPPORTED, TB_ERR_CUDA = range(7)
+TB_F32, TB_F16, TB_BF16 = 0, 1, 2
+TB_MAX_TILES_PER_AXIS = 64
+TB_MAX_TILES = 1024
+
+_DTYPES = {torch.float32: TB_F32, torch.float16: TB_F16, torch.bfloat16: TB_BF16}
+
+
+class tb_axis(ctypes.Structure):
+    _fields_ = [("latent_extent", ctypes.c_int32), ("latent_tile", ctypes.c_int32), ("overlap", ctypes.c_double),
+                ("scale", ctypes.c_int32), ("blend_extent", ctypes.c_int32), ("row_limit", ctypes.c_int32)]
+
+
+class tb_gn_partial(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("mean", ctypes.c_float), ("m2", ctypes.c_float)]
+
+
+_vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+_P_vp = ctypes.POINTER(ctypes.c_void_p)
+_P_i32 = ctypes.POINTER(ctypes.c_int32)
+_P_i64 = ctypes.POINTER(ctypes.c_int64)
+_P_axis = ctypes.POINTER(tb_axis)
+
+_lib.tb_version.restype = ctypes.c_size_t
+_lib.tb_version.argtypes = []
+_lib.tb_status_string.restype = ctypes.c_char_p
+_lib.tb_status_string.argtypes = [ctypes.c_int]
+_lib.tb_last_cuda_error.restype = ctypes.c_int
+_lib.tb_last_cuda_error.argtypes = []
+_lib.tb_axis_layout.restype = ctypes.c_int
+_lib.tb_axis_layout.argtypes = [_P_axis, _i32, _P_i32, _P_i64, _P_i32, _P_i32, _P_i32, _P_i64]
+_lib.tb_stitch2d.restype = ctypes.c_int
+_lib.tb_stitch2d.argtypes = [_P_vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _vp, _i64, _i64, _vp]
+_lib.tb_stitch3d.restype = ctypes.c_int
+_lib.tb_stitch3d.argtypes = [_P_vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _P_axis, _vp, _i64, _i64, _i64, _vp]
+_lib.tb_patch_gn_stats.restype = ctypes.c_int
+_lib.tb_patch_gn_stats.argtypes = [_P_vp, _i32, ctypes.c_int, _i64, _i64, _P_i64, _i32, _vp, _vp]
+_lib.tb_patch_gn_apply.restype = ctypes.c_int
+_lib.tb_patch_gn_apply.argtypes = [_P_vp, _P_vp, _i32, ctypes.c_int, _i64, _i64, _P_i64, _i32, _vp, _vp, _vp,
+                                   ctypes.c_float, _i32, _vp]
+
+EXPORTED = ("tb_version", "tb_status_string", "tb_last_cuda_error", "tb_axis_layout", "tb_stitch2d",
+            "tb_stitch3d", "tb_patch_gn_stats", "tb_patch_gn_apply")
+
+
+class TileBlendError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = "%s: %s" % (where, _lib.tb_status_string(status).decode())
+        if status == TB_ERR_CUDA:
+            msg += " (cudaError %d)" % _lib.tb_last_cuda_error()
+        super().__init__(msg)
+        self.status = status
+
+
+def _check(status: int, where: str) -> None:
+    if status != TB_OK:
+        raise TileBlendError(status, where)
+
+
+def tb_version() -> int:
+    return int(_lib.tb_version())
+
+
+# ---------------------------------------------------------------------------
+# geometry
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class Axis:
+    """Tile-grid parameters of one axis (see tb_axis in tileblend.h)."""
+    latent_extent: int
+    latent_tile: int
+    overlap: float
+    scale: int
+    blend_extent: int = -1   # < 0: stock value
+    row_limit: int = 0       # <= 0: stock value
+
+    def c(self) -> tb_axis:
+        return tb_axis(self.latent_extent, self.latent_tile, float(self.overlap), self.scale,
+                       self.blend_extent, self.row_limit)
+
+
+@dataclass(frozen=True)
+class Layout:
+    n: int
+    origins: List[int]     # in decoded samples
+    extents: List[int]
+    blends: List[int]
+    kept: List[int]
+    out_extent: int
+
+
+def tb_axis_layout(axis: Axis) -> Layout:
+    """The library's derived geometry of one axis (host only)."""
+    a = axis.c()
+    n = ctypes.c_int32(0)
+    cap = TB_MAX_TILES_PER_AXIS
+    org = (ctypes.c_int64 * cap)()
+    ext, bl, kp = (ctypes.c_int32 * cap)(), (ctypes.c_int32 * cap)(), (ctypes.c_int32 * cap)()
+    out = ctypes.c_int64(0)
+    _check(_lib.tb_axis_layout(ctypes.byref(a), cap, ctypes.byref(n), org, ext, bl, kp, ctypes.byref(out)),
+           "tb_axis_layout")
+    k = n.value
+    return Layout(k, list(org[:k]), list(ext[:k]), list(bl[:k]), list(kp[:k]), out.value)
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+    return _DTYPES[t.dtype]
+
+
+def _cuda_contig(t: torch.Tensor, what: str) -> None:
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+
+
+def _ptr_array(ptrs: Sequence[int]):
+    return (ctypes.c_void_p * max(1, len(ptrs)))(*ptrs)
+
+
+# ---------------------------------------------------------------------------
+# stitch
+# ---------------------------------------------------------------------------
+
+def tb_stitch2d(tiles: Sequence[Sequence[torch.Tensor]], ay: Axis, ax: Axis, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Stitch ``tiles[i][j]`` ([B, C, L_y(i), L_x(j)]) into ``out`` ([B, C, H, W])."""
+    _cuda_contig(out, "out")
+    B, C, H, W = out.shape
+    ly, lx = tb_axis_layout(ay), tb_axis_layout(ax)
+    ptrs = []
+    if len(tiles) != ly.n:
+        raise ValueError("expected %d tile rows, got %d" % (ly.n, len(tiles)))
+    for i, row in enumerate(tiles):
+        if len(row) != lx.n:
+            raise ValueError("expected %d tiles in row %d, got %d" % (lx.n, i, len(row)))
+        for j, t in enumerate(row):
+            _cuda_contig(t, "tile (%d,%d)" % (i, j))
+            if t.dtype != out.dtype or tuple(t.shape) != (B, C, ly.extents[i], lx.extents[j]):
+                raise ValueError("tile (%d,%d) has %s %s, expected %s %s" % (
+                    i, j, t.dtype, tuple(t.shape), out.dtype, (B, C, ly.extents[i], lx.extents[j])))
+            ptrs.append(t.data_ptr())
+    a_y, a_x = ay.c(), ax.c()
+    _check(_lib.tb_stitch2d(_ptr_array(ptrs), _dtype_code(out), B, C, ctypes.byref(a_y), ctypes.byref(a_x),
+                            out.data_ptr(), H, W, _stream_handle(stream)), "tb_stitch2d")
+    return out
+
+
+def tb_stitch3d(tiles, at: Axis, ay: Axis, ax: Axis, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Stitch ``tiles[k][i][j]`` ([B, C, L_t(k), L_y(i), L_x(j)]) into ``out``
+    ([B, C, T, H, W])."""
+    _cuda_contig(out, "out")
+    B, C, T, H, W = out.shape
+    lt, ly, lx = tb_axis_layout(at), tb_axis_layout(ay), tb_axis_layout(ax)
+    ptrs = []
+    if len(tiles) != lt.n:
+        raise ValueError("expected %d frame tiles, got %d" % (lt.n, len(tiles)))
+    for k, plane in enumerate(tiles):
+        if len(plane) != ly.n:
+            raise ValueError("expected %d tile rows" % ly.n)
+        for i, row in enumerate(plane):
+            if len(row) != lx.n:
+                raise ValueError("expected %d tiles per row" % lx.n)
+            for j, t in enumerate(row):
+                _cuda_contig(t, "tile (%d,%d,%d)" % (k, i, j))
+                exp = (B, C, lt.extents[k], ly.extents[i], lx.extents[j])
+                if t.dtype != out.dtype or tuple(t.shape) != exp:
+                    raise ValueError("tile (%d,%d,%d) has %s %s, expected %s %s" % (
+                        k, i, j, t.dtype, tuple(t.shape), out.dtype, exp))
+                ptrs.append(t.data_ptr())
+    a_t, a_y, a_x = at.c(), ay.c(), ax.c()
+    _check(_lib.tb_stitch3d(_ptr_array(ptrs), _dtype_code(out), B, C, ctypes.byref(a_t), ctypes.byref(a_y),
+                            ctypes.byref(a_x), out.data_ptr(), T, H, W, _stream_handle(stream)), "tb_stitch3d")
+    return out
+
+
+def tb_stitch2d_raw(tile_ptrs: Sequence[int], dtype: int, B: int, C: int, ay: Axis, ax: Axis, out_ptr: int,
+                    H: int, W: int, stream=None) -> None:
+    """Pointer-level call (no tensor checks), for timing the bare C ABI."""
+    a_y, a_x = ay.c(), ax.c()
+    _check(_lib.tb_stitch2d(_ptr_array(tile_ptrs), dtype, B, C, ctypes.byref(a_y), ctypes.byref(a_x), out_ptr,
+                            H, W, _stream_handle(stream)), "tb_stitch2d")
+
+
+# ---------------------------------------------------------------------------
+# PatchGroupNorm
+# ---------------------------------------------------------------------------
+
+def _gn_args(patches: Sequence[torch.Tensor]) -> Tuple[int, int, int, list, list]:
+    if len(patches) == 0:
+        raise ValueError("at least one patch")
+    N, C = patches[0].shape[:2]
+    spatial = []
+    ptrs = []
+    for q, t in enumerate(patches):
+        _cuda_contig(t, "patch %d" % q)
+        if t.dtype != patches[0].dtype or tuple(t.shape[:2]) != (N, C):
+            raise ValueError("patch %d: dtype/leading dims differ from patch 0" % q)
+        s = 1
+        for d in t.shape[2:]:
+            s *= d
+        spatial.append(s)
+        ptrs.append(t.data_ptr())
+    return N, C, _dtype_code(patches[0]), spatial, ptrs
+
+
+def new_partials(P: int, N: int, G: int, device=None) -> torch.Tensor:
+    """Device buffer for P * N * G tb_gn_partial records (16 bytes each)."""
+    return torch.empty((P, N, G, 2), dtype=torch.int64, device=device or torch.device("cuda"))
+
+
+def tb_patch_gn_stats(patches: Sequence[torch.Tensor], G: int, partials: torch.Tensor, stream=None) -> torch.Tensor:
+    """Per-patch (count, mean, M2) of every (sample, group) into ``partials``
+    (a [P, N, G, 2] int64 buffer from ``new_partials``)."""
+    N, C, dt, spatial, ptrs = _gn_args(patches)
+    P = len(patches)
+    _cuda_contig(partials, "partials")
+    if partials.numel() * partials.element_size() != P * N * G * 16:
+        raise ValueError("partials must hold P*N*G 16-byte records")
+    sp = (ctypes.c_int64 * P)(*spatial)
+    _check(_lib.tb_patch_gn_stats(_ptr_array(ptrs), P, dt, N, C, sp, G, partials.data_ptr(), _stream_handle(stream)),
+           "tb_patch_gn_stats")
+    return partials
+
+
+def tb_patch_gn_apply(patches: Sequence[torch.Tensor], outs: Sequence[torch.Tensor], G: int, partials: torch.Tensor,
+                      gamma: Optional[torch.Tensor], beta: Optional[torch.Tensor], eps: float, silu: bool = True,
+                      stream=None) -> Sequence[torch.Tensor]:
+    """Normalise every patch with the pooled statistics of ``partials``;
+    ``outs[p]`` may be ``patches[p]``."""
+    N, C, dt, spatial, ptrs = _gn_args(patches)
+    P = len(patches)
+    if len(outs) != P:
+        raise ValueError("one output per patch")
+    optrs = []
+    for q, (o, t) in enumerate(zip(outs, patches)):
+        _cuda_contig(o, "out %d" % q)
+        if o.shape != t.shape or o.dtype != t.dtype:
+            raise ValueError("out %d must match patch %d" % (q, q))
+        optrs.append(o.data_ptr())
+    for name, v in (("gamma", gamma), ("beta", beta)):
+        if v is not None:
+            _cuda_contig(v, name)
+            if v.numel() != C or v.dtype != patches[0].dtype:
+                raise ValueError("%s must be [C] of the patches' dtype" % name)
+    _cuda_contig(partials, "partials")
+    if partials.numel() * partials.element_size() != P * N * G * 16:
+        raise ValueError("partials must hold P*N*G 16-byte records")
+    sp = (ctypes.c_int64 * P)(*spatial)
+    _check(_lib.tb_patch_gn_apply(_ptr_array(ptrs), _ptr_array(optrs), P, dt, N, C, sp, G, partials.data_ptr(),
+                                  gamma.data_ptr() if gamma is not None else None,
+                                  beta.data_ptr() if beta is not None else None, float(eps), 1 if silu else 0,
+                                  _stream_handle(stream)), "tb_patch_gn_apply")
+    return outs
+
+
+def patch_group_norm(patches: Sequence[torch.Tensor], G: int, gamma, beta, eps: float, silu: bool = True,
+                     outs: Optional[Sequence[torch.Tensor]] = None, partials: Optional[torch.Tensor] = None,
+                     stream=None) -> Sequence[torch.Tensor]:
+    """Both steps: statistics of every patch, then the pooled normalisation."""
+    N = patches[0].shape[0]
+    if partials is None:
+        partials = new_partials(len(patches), N, G, patches[0].device)
+    if outs is None:
+        outs = [torch.empty_like(p) for p in patches]
+    tb_patch_gn_stats(patches, G, partials, stream)
+    return tb_patch_gn_apply(patches, outs, G, partials, gamma, beta, eps, silu, stream)

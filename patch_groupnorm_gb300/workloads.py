@@ -1,0 +1,98 @@
+"""Named synthetic workloads: tile-grid parameters, shapes and input recipe.
+
+Each stitch workload is a decoded image or clip cut into overlapping tiles by
+the stock tiled-decode rule (latent tile, overlap factor, latent scale); the
+tiles are drawn by ``synth``.  The PatchGroupNorm workloads are decoder
+activations split into four patches along one spatial axis.
+
+The generator needs each tile's placement (output-space origin, extent);
+callers pass it from a derived geometry -- ``tileblend.tb_axis_layout`` in
+the product path, the oracle's geometry in the tests.
+"""
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence, Tuple
+
+from . import synth
+
+
+@dataclass(frozen=True)
+class AxisSpec:
+    latent_extent: int
+    latent_tile: int
+    overlap: float
+    scale: int
+
+
+@dataclass(frozen=True)
+class StitchWorkload:
+    name: str
+    dtype: str                 # 'f32' | 'f16' | 'bf16'
+    B: int
+    C: int
+    axes: Tuple[AxisSpec, ...]  # (y, x) or (t, y, x)
+    recipe: str                # 'smooth' | 'uniform' | 'spacetime'
+    seed: int
+
+    @property
+    def ndim(self) -> int:
+        return len(self.axes)
+
+
+def _img(extent_lat, tile=64, ov=0.25, scale=8):
+    return AxisSpec(extent_lat, tile, ov, scale)
+
+
+STITCH = {
+    # 2D, fp32, 1024x1024, 3x3 grid of 512 px tiles (blend 128, row_limit 384)
+    "image_1024_f32": StitchWorkload("image_1024_f32", "f32", 1, 3, (_img(128), _img(128)), "smooth", 1234),
+    # 2D, batch 4, 2048x2048, 6x6 grid, last tiles 128 px
+    "image_2048_f16": StitchWorkload("image_2048_f16", "f16", 4, 3, (_img(256), _img(256)), "smooth", 1235),
+    "image_2048_bf16": StitchWorkload("image_2048_bf16", "bf16", 4, 3, (_img(256), _img(256)), "smooth", 1235),
+    "image_2048_f16_uniform": StitchWorkload("image_2048_f16_uniform", "f16", 4, 3, (_img(256), _img(256)),
+                                             "uniform", 1335),
+    "image_2048_bf16_uniform": StitchWorkload("image_2048_bf16_uniform", "bf16", 4, 3, (_img(256), _img(256)),
+                                              "uniform", 1335),
+    # 2D, 1600x2048 (latent 200x256), 120x72-latent tiles: per-axis blends, clamped slivers
+    "wide_1600x2048_bf16": StitchWorkload("wide_1600x2048_bf16", "bf16", 1, 3, (_img(200, 120), _img(256, 72)),
+                                          "smooth", 1236),
+    # 3D, 49 frames of 480x832: 16-frame tiles (stride 12, blend 4), 256 px tiles (stride 192, blend 64)
+    "video_49x480x832_bf16": StitchWorkload("video_49x480x832_bf16", "bf16", 1, 3,
+                                            (AxisSpec(49, 16, 0.25, 1), _img(60, 32), _img(104, 32)),
+                                            "spacetime", 1237),
+}
+
+
+@dataclass(frozen=True)
+class GroupNormWorkload:
+    name: str
+    dtype: str
+    shape: Tuple[int, ...]     # unsharded [N, C, *spatial]
+    split_dim: int
+    patches: int
+    patch_means: Tuple[float, ...]
+    groups: int
+    eps: float
+    seed: int
+
+
+GROUPNORM = {
+    "gn_4d_1x512x256x256": GroupNormWorkload("gn_4d_1x512x256x256", "bf16", (1, 512, 256, 256), 2, 4,
+                                             (-3.0, -1.0, 1.0, 3.0), 32, 1e-6, 1238),
+    "gn_5d_1x384x13x120x208": GroupNormWorkload("gn_5d_1x384x13x120x208", "bf16", (1, 384, 13, 120, 208), 4, 4,
+                                                (-3.0, -1.0, 1.0, 3.0), 32, 1e-6, 1239),
+}
+
+
+def make_stitch_tiles(w: StitchWorkload, boxes: Sequence[Sequence[Tuple[int, int]]], out_extents: Sequence[int]):
+    """CPU tiles of workload ``w``; ``boxes[a]`` lists (origin, extent) of the
+    tiles along axis a and ``out_extents`` the output extents."""
+    bx = boxes
+    if w.ndim == 2:
+        if w.recipe == "uniform":
+            return synth.uniform_tiles(w.seed, w.B, w.C, bx[0], bx[1], w.dtype)
+        return synth.smooth_field_tiles(w.seed, w.B, w.C, tuple(out_extents), bx[0], bx[1], w.dtype)
+    return synth.spacetime_field_tiles(w.seed, w.B, w.C, tuple(out_extents), bx[0], bx[1], bx[2], w.dtype)
+
+
+def make_groupnorm_inputs(w: GroupNormWorkload):
+    return synth.groupnorm_patches(w.seed, w.shape, w.split_dim, w.patches, w.patch_means, w.dtype)

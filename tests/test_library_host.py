@@ -1,0 +1,165 @@
+"""CPU-only checks of libtileblend: it builds, loads, exports every call the
+header declares, derives the same geometry as the oracle, and rejects bad
+arguments on the host before touching a GPU."""
+import ctypes
+import json
+import os
+import random
+import re
+
+import pytest
+
+from oracle.geometry import axis_layout
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tileblend.h")
+
+
+@pytest.fixture(scope="module")
+def tbl():
+    from patch_groupnorm_gb300 import build
+    build.build()
+    from patch_groupnorm_gb300 import tileblend
+    return tileblend
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tb_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    assert set(_declared_functions()) >= {"tb_stitch2d", "tb_stitch3d", "tb_patch_gn_stats", "tb_patch_gn_apply"}
+
+
+def test_library_exports_every_declared_symbol(tbl):
+    lib = ctypes.CDLL(tbl.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_declared_functions()) == set(tbl.EXPORTED)
+
+
+def test_library_exports_nothing_else(tbl):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", tbl.LIB_PATH], capture_output=True, text=True).stdout
+    ours = sorted(l.split()[-1] for l in out.splitlines() if l.split()[-1].startswith("tb_"))
+    assert ours == _declared_functions()
+
+
+def test_version(tbl):
+    assert tbl.tb_version() >= 100
+
+
+GOLDEN = json.load(open(os.path.join(ROOT, "tests", "golden", "geometry.json")))["cases"]
+
+
+@pytest.mark.parametrize("case", GOLDEN, ids=[c["name"] for c in GOLDEN])
+def test_layout_matches_golden(tbl, case):
+    lay = tbl.tb_axis_layout(tbl.Axis(case["latent_extent"], case["latent_tile"], case["overlap"], case["scale"]))
+    assert lay.extents == case["extents"]
+    assert lay.blends == case["blends"]
+    assert lay.kept == case["kept"]
+    assert lay.out_extent == case["out_extent"]
+
+
+def test_layout_matches_oracle_on_random_axes(tbl):
+    rnd = random.Random(7)
+    for _ in range(3000):
+        tile = rnd.randint(1, 160)
+        ov = rnd.choice([0.0, 0.125, 0.2, 0.25, 0.3, 1 / 3, 0.5, 0.6, 0.75, rnd.random() * 0.95])
+        if int(tile * (1 - ov)) < 1:
+            continue
+        ext = rnd.randint(0, 40 * max(1, int(tile * (1 - ov))))
+        scale = rnd.choice([1, 2, 4, 8, 16])
+        be = rnd.choice([None, None, rnd.randint(0, 300)])
+        rl = rnd.choice([None, None, rnd.randint(1, 900)])
+        o = axis_layout(ext, tile, ov, scale, be, rl)
+        if o.n > tbl.TB_MAX_TILES_PER_AXIS:
+            continue
+        if o.row_limit < 1:
+            continue
+        lay = tbl.tb_axis_layout(tbl.Axis(ext, tile, ov, scale, -1 if be is None else be, 0 if rl is None else rl))
+        assert (lay.n, lay.extents, lay.blends, lay.kept, lay.out_extent) == \
+               (o.n, o.extents, o.blends, o.kept, o.out_extent), (ext, tile, ov, scale, be, rl)
+        assert lay.origins == [v * scale for v in o.origins]
+
+
+@pytest.mark.parametrize("bad", [
+    dict(latent_extent=-1), dict(latent_tile=0), dict(scale=0), dict(overlap=1.0), dict(overlap=-0.1),
+    dict(overlap=float("nan")), dict(latent_tile=1, overlap=0.5),  # zero stride
+    dict(blend_extent=600, row_limit=0),                           # derived row_limit < 1
+])
+def test_layout_rejects_bad_geometry(tbl, bad):
+    kw = dict(latent_extent=128, latent_tile=64, overlap=0.25, scale=8, blend_extent=-1, row_limit=0)
+    kw.update(bad)
+    with pytest.raises(tbl.TileBlendError) as e:
+        tbl.tb_axis_layout(tbl.Axis(**kw))
+    assert e.value.status == tbl.TB_ERR_GEOMETRY
+
+
+def test_layout_too_many_tiles_is_unsupported_and_reports_count(tbl):
+    a = tbl.Axis(1000, 8, 0.5, 8).c()
+    n = ctypes.c_int32(0)
+    st = tbl._lib.tb_axis_layout(ctypes.byref(a), 0, ctypes.byref(n), None, None, None, None, None)
+    assert st == tbl.TB_ERR_UNSUPPORTED and n.value == 250
+
+
+# --- host-side validation of the compute calls: no GPU is touched -----------
+
+def _stitch2d(tbl, dtype=0, B=1, C=3, ay=None, ax=None, H=1024, W=1024, tiles="ok", out=16):
+    ay = ay or tbl.Axis(128, 64, 0.25, 8)
+    ax = ax or tbl.Axis(128, 64, 0.25, 8)
+    arr = (ctypes.c_void_p * 256)(*([16 * (k + 1) for k in range(256)])) if tiles == "ok" else tiles
+    a_y, a_x = ay.c(), ax.c()
+    return tbl._lib.tb_stitch2d(arr, dtype, B, C, ctypes.byref(a_y), ctypes.byref(a_x), out, H, W, None)
+
+
+def test_stitch_rejects_before_launch(tbl):
+    assert _stitch2d(tbl, dtype=7) == tbl.TB_ERR_DTYPE
+    assert _stitch2d(tbl, H=1000) == tbl.TB_ERR_SHAPE
+    assert _stitch2d(tbl, W=-1) == tbl.TB_ERR_SHAPE
+    assert _stitch2d(tbl, B=-2) == tbl.TB_ERR_SHAPE
+    assert _stitch2d(tbl, out=None) == tbl.TB_ERR_NULL
+    assert _stitch2d(tbl, tiles=None) == tbl.TB_ERR_NULL
+    nulls = (ctypes.c_void_p * 9)(*([16] * 8 + [None]))
+    assert _stitch2d(tbl, tiles=nulls) == tbl.TB_ERR_NULL
+    assert _stitch2d(tbl, ay=tbl.Axis(128, 64, 1.5, 8)) == tbl.TB_ERR_GEOMETRY
+    # bands that reach each other (overlap 3/4): outside the closed form
+    chain = tbl.Axis(128, 64, 0.75, 8)
+    lay = axis_layout(128, 64, 0.75, 8)
+    assert _stitch2d(tbl, ay=chain, H=lay.out_extent) == tbl.TB_ERR_UNSUPPORTED
+    # nothing to do: no launch, success, even with null pointers
+    assert _stitch2d(tbl, B=0, tiles=None, out=None) == tbl.TB_OK
+    assert _stitch2d(tbl, ay=tbl.Axis(0, 64, 0.25, 8), H=0, tiles=None, out=None) == tbl.TB_OK
+
+
+def test_stitch3d_rejects_before_launch(tbl):
+    at, ay, ax = tbl.Axis(49, 16, 0.25, 1).c(), tbl.Axis(60, 32, 0.25, 8).c(), tbl.Axis(104, 32, 0.25, 8).c()
+    arr = (ctypes.c_void_p * 75)(*([16] * 75))
+    f = tbl._lib.tb_stitch3d
+    assert f(arr, 2, 1, 3, None, ctypes.byref(ay), ctypes.byref(ax), 16, 49, 480, 832, None) == tbl.TB_ERR_NULL
+    assert f(arr, 2, 1, 3, ctypes.byref(at), ctypes.byref(ay), ctypes.byref(ax), 16, 48, 480, 832, None) \
+        == tbl.TB_ERR_SHAPE
+
+
+def test_groupnorm_rejects_before_launch(tbl):
+    ptrs = (ctypes.c_void_p * 4)(16, 32, 48, 64)
+    sp = (ctypes.c_int64 * 4)(100, 100, 100, 100)
+    f = tbl._lib.tb_patch_gn_stats
+    assert f(ptrs, 4, 9, 1, 64, sp, 32, 16, None) == tbl.TB_ERR_DTYPE
+    assert f(ptrs, 4, 2, 1, 60, sp, 32, 16, None) == tbl.TB_ERR_SHAPE        # C % G
+    assert f(ptrs, 0, 2, 1, 64, sp, 32, 16, None) == tbl.TB_ERR_SHAPE        # P < 1
+    assert f(ptrs, 4, 2, 1, 64, sp, 32, None, None) == tbl.TB_ERR_NULL       # partials
+    assert f(ptrs, 4, 2, 1, 64, None, 32, 16, None) == tbl.TB_ERR_NULL       # spatial
+    assert f(ptrs, 65, 2, 1, 64, (ctypes.c_int64 * 65)(*[1] * 65), 32, 16, None) == tbl.TB_ERR_UNSUPPORTED
+    g = tbl._lib.tb_patch_gn_apply
+    assert g(ptrs, ptrs, 4, 2, 1, 64, sp, 32, 16, None, None, ctypes.c_float(-1.0), 1, None) == tbl.TB_ERR_SHAPE
+    assert g(ptrs, None, 4, 2, 1, 64, sp, 32, 16, None, None, ctypes.c_float(1e-6), 1, None) == tbl.TB_ERR_NULL
+    assert g(ptrs, ptrs, 4, 2, 0, 64, sp, 32, 16, None, None, ctypes.c_float(1e-6), 1, None) == tbl.TB_OK
+
+
+def test_status_strings(tbl):
+    for s in range(7):
+        assert tbl._lib.tb_status_string(s)
+    assert tbl._lib.tb_status_string(99) == b"unknown status"
