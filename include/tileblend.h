@@ -223,6 +223,42 @@ tb_status tb_patch_gn_apply(const void* const* patches, void* const* outs, int32
                             int64_t C, const int64_t* spatial, int32_t G, const tb_gn_partial* partials,
                             const void* gamma, const void* beta, float eps, int32_t silu, void* stream);
 
+/*
+ * tb_patch_group_norm_noalloc -- PatchGroupNorm (statistics, then pooled
+ * normalisation, affine and optional SiLU) for callers that cannot allocate
+ * device memory.  The pages have no counterpart: it exists for this
+ * library's users.
+ *
+ * Some callers may not call cudaMalloc at all: code embedded in a host
+ * framework that owns every device allocation through its own memory pool,
+ * or code on a latency-critical path where an allocation (which can
+ * synchronise the device) is not allowed.  Such a caller still owns the
+ * inputs and outputs, but cannot provide the partials buffer that
+ * tb_patch_gn_stats / tb_patch_gn_apply exchange.  This call keeps those
+ * partials in a fixed scratch array compiled into the library instead
+ * (TB_NOALLOC_MAX_PARTIALS records of 16 bytes, 1 MiB, held on every GPU
+ * that loads the library until the process exits) and allocates nothing.
+ *
+ * Arguments and results are those of tb_patch_gn_apply, minus `partials`.
+ * The result equals tb_patch_gn_stats followed by tb_patch_gn_apply.
+ *
+ *   - P * N * G larger than TB_NOALLOC_MAX_PARTIALS returns
+ *     TB_ERR_UNSUPPORTED and launches nothing.
+ *   - The first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress, with that device current); make that
+ *     first call before any stream capture.
+ *   - Every call uses the same scratch array.  Each call writes every record
+ *     it reads before reading it, so nothing needs clearing, but two calls
+ *     whose work overlaps on the GPU (different streams, or different host
+ *     threads, without ordering between them) race on the array and may give
+ *     wrong results.  Order such calls on one stream.
+ * Errors as tb_patch_gn_apply; TB_ERR_CUDA also if the address lookup fails.
+ */
+#define TB_NOALLOC_MAX_PARTIALS 65536
+tb_status tb_patch_group_norm_noalloc(const void* const* patches, void* const* outs, int32_t P, tb_dtype dtype,
+                                      int64_t N, int64_t C, const int64_t* spatial, int32_t G, const void* gamma,
+                                      const void* beta, float eps, int32_t silu, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,6 +25,7 @@ UNITS = {
     "tb_host.cpp": [],
     "tb_stitch.cu": ["-fmad=false"],
     "tb_groupnorm.cu": [],
+    "tb_noalloc.cu": [],
 }
 HEADERS = ["tb_internal.h"]
 

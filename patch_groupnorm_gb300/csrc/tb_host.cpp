@@ -324,6 +324,8 @@ tb_status gn_validate(const void* const* patches, int32_t P, tb_dtype dtype, int
 
 }  // namespace
 
+void tb::record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
 // ===========================================================================
 // C ABI
 // ===========================================================================

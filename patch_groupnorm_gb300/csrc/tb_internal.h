@@ -109,6 +109,9 @@ struct GnApplyParams {
 // on whether the 16-byte vector path is taken.
 int gn_apply_segment(int dtype, bool aligned);
 
+// Records a CUDA error for tb_last_cuda_error() (defined in tb_host.cpp).
+void record_cuda_error(cudaError_t e);
+
 cudaError_t launch_gn_stats(const GnStatsParams& p, int dtype, int64_t units, cudaStream_t s);
 cudaError_t launch_gn_apply(const GnApplyParams& p, int dtype, int64_t items, cudaStream_t s);
 

@@ -72,8 +72,13 @@ _lib.tb_patch_gn_apply.restype = ctypes.c_int
 _lib.tb_patch_gn_apply.argtypes = [_P_vp, _P_vp, _i32, ctypes.c_int, _i64, _i64, _P_i64, _i32, _vp, _vp, _vp,
                                    ctypes.c_float, _i32, _vp]
 
+_lib.tb_patch_group_norm_noalloc.restype = ctypes.c_int
+_lib.tb_patch_group_norm_noalloc.argtypes = [_P_vp, _P_vp, _i32, ctypes.c_int, _i64, _i64, _P_i64, _i32, _vp, _vp,
+                                             ctypes.c_float, _i32, _vp]
+TB_NOALLOC_MAX_PARTIALS = 65536
+
 EXPORTED = ("tb_version", "tb_status_string", "tb_last_cuda_error", "tb_axis_layout", "tb_stitch2d",
-            "tb_stitch3d", "tb_patch_gn_stats", "tb_patch_gn_apply")
+            "tb_stitch3d", "tb_patch_gn_stats", "tb_patch_gn_apply", "tb_patch_group_norm_noalloc")
 
 
 class TileBlendError(RuntimeError):
@@ -312,3 +317,36 @@ def patch_group_norm(patches: Sequence[torch.Tensor], G: int, gamma, beta, eps: 
         outs = [torch.empty_like(p) for p in patches]
     tb_patch_gn_stats(patches, G, partials, stream)
     return tb_patch_gn_apply(patches, outs, G, partials, gamma, beta, eps, silu, stream)
+
+
+def tb_patch_group_norm_noalloc(patches: Sequence[torch.Tensor], outs: Sequence[torch.Tensor], G: int,
+                                gamma: Optional[torch.Tensor], beta: Optional[torch.Tensor], eps: float,
+                                silu: bool = True, stream=None) -> Sequence[torch.Tensor]:
+    """PatchGroupNorm for callers that cannot allocate device memory: the
+    partial statistics live in the library's own fixed scratch array
+    (at most TB_NOALLOC_MAX_PARTIALS = P * N * G records), so the call needs
+    no buffer besides the inputs and outputs.  Calls share that array: order
+    them on one stream.  The first call on a device looks the array up; make
+    it before any stream capture."""
+    N, C, dt, spatial, ptrs = _gn_args(patches)
+    P = len(patches)
+    if len(outs) != P:
+        raise ValueError("one output per patch")
+    optrs = []
+    for q, (o, t) in enumerate(zip(outs, patches)):
+        _cuda_contig(o, "out %d" % q)
+        if o.shape != t.shape or o.dtype != t.dtype:
+            raise ValueError("out %d must match patch %d" % (q, q))
+        optrs.append(o.data_ptr())
+    for name, v in (("gamma", gamma), ("beta", beta)):
+        if v is not None:
+            _cuda_contig(v, name)
+            if v.numel() != C or v.dtype != patches[0].dtype:
+                raise ValueError("%s must be [C] of the patches' dtype" % name)
+    sp = (ctypes.c_int64 * P)(*spatial)
+    _check(_lib.tb_patch_group_norm_noalloc(_ptr_array(ptrs), _ptr_array(optrs), P, dt, N, C, sp, G,
+                                            gamma.data_ptr() if gamma is not None else None,
+                                            beta.data_ptr() if beta is not None else None, float(eps),
+                                            1 if silu else 0, _stream_handle(stream)),
+           "tb_patch_group_norm_noalloc")
+    return outs
