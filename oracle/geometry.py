@@ -15,8 +15,9 @@ Their plainest reading, the one the tiled decode in diffusers uses, is:
     blend_extent  = int(latent_tile * scale * overlap)           (px)
     row_limit     = latent_tile * scale - blend_extent           (px)
 
-Per pair of neighbouring tiles the blend is clamped ("preserving clamping",
-page "[Proposal] Vectorize tiled VAE blending ...", "Proposed scope"):
+Per pair of neighbouring tiles the blend extent is clamped to what both
+tiles hold (page "[Proposal] Vectorize tiled VAE blending ...", "Proposed
+scope", which keeps that clamp when vectorising):
 
     e(n) = min(extent(n-1), extent(n), blend_extent),   e(0) = 0
 

@@ -20,9 +20,10 @@
  * Afterwards every tile is cropped to its first row_limit slices per axis
  * and the crops are concatenated.
  *
- * Rounding (the same page: "preserving ... per-product rounding" and
- * "float64 tensor division to match Python-double rounding"): the two
- * coefficients are computed in double precision and used as fp32 scalars;
+ * Rounding (the same page, same section: each product is rounded on its
+ * own, and the coefficients come from double-precision division so that
+ * they equal Python's float quotients): the two coefficients are computed
+ * in double precision and used as fp32 scalars;
  * each product is one fp32 multiply rounded to the storage type; the sum of
  * the two rounded products is one fp32 add rounded to the storage type.
  * Round-to-nearest-even into fp16 and bf16 is written out below from the

@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
 
 Thin ctypes marshalling around ``orc_stitch`` in ``stitch.c``, which holds the
 arithmetic (the page "[Proposal] Vectorize tiled VAE blending while
-preserving rounding and CUDA graph replay", "Proposed scope": blend loops
-with clamping, in-place output and per-product rounding).
+preserving rounding and CUDA graph replay", "Proposed scope": the blend
+loops, their extent clamp, their in-place updates and their rounding of
+each product separately).
 
 Tiles are numpy arrays in raw storage form: float32 for 'f32', float64 for
 'f64', and uint16 bit patterns for 'f16' / 'bf16'.

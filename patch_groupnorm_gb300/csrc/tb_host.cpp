@@ -11,9 +11,9 @@
 //     L(n) = min(latent_tile, latent_extent - origin) * scale
 //     blend_extent = int(latent_tile * scale * overlap),  row_limit = tile - blend_extent
 //     e(n) = min(L(n-1), L(n), blend_extent),  K(n) = min(L(n), row_limit)
-// The blend coefficients are the pages' Python-double quotients c/e and
-// 1 - c/e, narrowed to fp32 ("float64 tensor division to match
-// Python-double rounding", same page), computed here once per distinct e.
+// The blend coefficients are the Python-double quotients c/e and 1 - c/e
+// narrowed to fp32 (the same page divides in float64 so that on-device
+// coefficients equal Python's), computed here once per distinct e.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
