@@ -25,6 +25,11 @@
 
 #define TB_API extern "C" __attribute__((visibility("default")))
 
+// Output rows per thread in one stitch work piece.
+#ifndef TB_STITCH_ROWS_PER_THREAD
+#define TB_STITCH_ROWS_PER_THREAD 16
+#endif
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
@@ -117,34 +122,6 @@ tb_status device_sms(int* sms) {
     return TB_OK;
 }
 
-// occupancy per (device, kernel variant, block size), cached
-struct OccKey {
-    int dev, ndim, dtype, vec, kx, block, large;
-};
-constexpr int OCC_CAP = 256;
-OccKey g_occ_key[OCC_CAP];
-int g_occ_val[OCC_CAP];
-int g_occ_n = 0;
-
-int stitch_occupancy(const tb::StitchLaunch& l, bool large) {
-    int dev = 0;
-    (void)cudaGetDevice(&dev);
-    std::lock_guard<std::mutex> lock(g_mu);
-    for (int q = 0; q < g_occ_n; ++q) {
-        const OccKey& k = g_occ_key[q];
-        if (k.dev == dev && k.ndim == l.ndim && k.dtype == l.dtype && k.vec == l.vec && k.kx == l.kx &&
-            k.block == l.block && k.large == (int)large)
-            return g_occ_val[q];
-    }
-    const int v = tb::stitch_kernel_max_ctas_per_sm(l, large);
-    if (g_occ_n < OCC_CAP) {
-        g_occ_key[g_occ_n] = OccKey{dev, l.ndim, l.dtype, l.vec, l.kx, l.block, (int)large};
-        g_occ_val[g_occ_n] = v;
-        ++g_occ_n;
-    }
-    return v;
-}
-
 int elem_bytes(tb_dtype d) { return d == TB_F32 ? 4 : 2; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -211,37 +188,33 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     for (int q = 0; ok && q < ntiles; ++q) ok = aligned16(tiles[q]);
     if (!ok) vec = 1;
 
+    prm.rows_per_thread = TB_STITCH_ROWS_PER_THREAD;
     tb::StitchLaunch l{};
     l.ndim = ndim;
     l.dtype = (int)dtype;
     l.vec = vec;
-    l.kx = 1;
-    const int64_t wc = prm.OW / vec;  // chunks per output row
-    int xt, nseg;
-    if (wc <= 512) {
-        xt = (int)wc;
-        nseg = 1;
-    } else {
-        xt = 256;
-        nseg = (int)((wc + xt * l.kx - 1) / (xt * l.kx));
-    }
-    const int rp = xt >= 256 ? 1 : (256 + xt - 1) / xt;
-    prm.xt = xt;
-    prm.rp = rp;
-    prm.nseg = nseg;
-    prm.seg_chunks = xt * l.kx;
-    const int64_t rows = planes * (int64_t)prm.OT * prm.OH;
-    prm.nvrows = rows * nseg;
-    if (prm.nvrows >= (int64_t)1 << 31) return TB_ERR_UNSUPPORTED;
-    l.block = xt * rp;
-
-    int sms = 0;
-    tb_status st = device_sms(&sms);
-    if (st != TB_OK) return st;
-    const int per_sm = stitch_occupancy(l, large);
-    const int64_t want = (prm.nvrows + rp - 1) / rp;
-    const int64_t cap = (int64_t)sms * per_sm;
-    l.grid = (int)(want < cap ? want : cap);
+    // pieces per tile: the grid's x extent is the largest
+    int max_pieces = 0, max_ebx = 0, max_eby = 0;
+    for (int k = 0; k < g[0].n; ++k)
+        for (int i = 0; i < g[1].n; ++i)
+            for (int j = 0; j < g[2].n; ++j) {
+                const int ebt = (ndim == 3 && k > 0) ? std::min(g[0].blend[k], g[0].kept[k]) : 0;
+                const int eby = i > 0 ? std::min(g[1].blend[i], g[1].kept[i]) : 0;
+                const int ebx = j > 0 ? std::min(g[2].blend[j], g[2].kept[j]) : 0;
+                max_ebx = std::max(max_ebx, ebx);
+                max_eby = std::max(max_eby, eby);
+                const int np = tb::tile_pieces(ndim, g[0].kept[k], g[1].kept[i], g[2].kept[j], ebt, eby, ebx, vec,
+                                               prm.rows_per_thread);
+                max_pieces = std::max(max_pieces, np);
+            }
+    if (max_pieces == 0) return TB_OK;
+    if ((int64_t)ntiles * planes > 2147483647LL || max_pieces > 65535) return TB_ERR_UNSUPPORTED;
+    l.grid_x = (int)(ntiles * planes);
+    l.grid_y = max_pieces;
+    l.grid_z = 1;
+    l.smem = (int)(sizeof(float) * 2 * (size_t)(max_ebx + max_eby));
+    if (l.smem > 200 * 1024) return TB_ERR_UNSUPPORTED;
+    (void)large;
 
     cudaError_t e;
     if constexpr (sizeof(P) == sizeof(tb::StitchParamsLarge)) {

@@ -31,13 +31,9 @@ struct StitchParams {
     const void* tiles[MAXT];   // row-major over (k, i, j)
     void* out;                 // [planes, OT, OH, OW]
     int64_t planes;            // B * C
-    int64_t nvrows;            // virtual rows = planes * OT * OH * nseg
     int32_t OT, OH, OW;        // output extents
-    int32_t nseg;              // row segments per output row (width split across virtual rows)
-    int32_t seg_chunks;        // chunks per segment (= XT * KX)
-    int32_t xt;                // threads per virtual row
-    int32_t rp;                // virtual rows per CTA pass (blockDim = xt * rp)
     int32_t ncoef;             // used entries of coef[]
+    int32_t rows_per_thread;   // work per thread in a box piece (tuning)
     StitchAxis<MAXA> ax[3];    // t, y, x
     float2 coef[MAXC];         // (w, u) = ((float)(c/e), (float)(1 - c/e)) per distinct e, c < e
 };
@@ -50,20 +46,79 @@ using StitchParamsLarge = StitchParams<LARGE_MAXA, LARGE_MAXT, LARGE_MAXC>;
 
 static_assert(sizeof(StitchParamsLarge) <= 32000, "kernel parameter block too large");
 
+constexpr int STITCH_BLOCK = 256;
+
+// The kept part of a tile splits into up to 2^d boxes by band membership:
+// box b has bit 2 set if it lies in the tile's time band, bit 1 in its
+// height band, bit 0 in its width band.  Inside a box every element is
+// computed from the same set of source tiles.  `eb*` are the band extents
+// clamped to the kept extents; widths are in chunks of `vec` elements.
+struct BoxShape {
+    int t0, nt, y0, ny, x0, width;
+};
+
+__host__ __device__ inline BoxShape box_shape(int b, int Kt, int Ky, int Kx, int ebt, int eby, int ebx, int vec) {
+    BoxShape s;
+    s.t0 = (b & 4) ? 0 : ebt;
+    s.nt = (b & 4) ? ebt : Kt - ebt;
+    s.y0 = (b & 2) ? 0 : eby;
+    s.ny = (b & 2) ? eby : Ky - eby;
+    s.x0 = (b & 1) ? 0 : ebx;
+    const int nx = (b & 1) ? ebx : Kx - ebx;
+    s.width = nx / vec;
+    return s;
+}
+
+// Thread layout of a CTA on a box `width` chunks wide: bdx threads across,
+// bdy rows at a time, each thread covering cpt columns.
+__host__ __device__ inline void box_layout(int width, int& bdx, int& bdy, int& cpt) {
+    bdx = width < STITCH_BLOCK ? width : STITCH_BLOCK;
+    if (bdx < 1) bdx = 1;
+    bdy = STITCH_BLOCK / bdx;
+    cpt = (width + bdx - 1) / bdx;
+}
+
+// Rows of box b one CTA processes (a "piece").  A box costs about one load
+// and one blend more per element for every band it lies in, so heavier boxes
+// get proportionally fewer rows per thread: pieces then take similar time.
+__host__ __device__ inline int box_piece_rows(int b, int width, int rows_per_thread) {
+    int bdx, bdy, cpt;
+    box_layout(width, bdx, bdy, cpt);
+    const int bands = (b & 1) + ((b >> 1) & 1) + ((b >> 2) & 1);
+    const int per = (rows_per_thread >> bands) / cpt;
+    return bdy * (per > 1 ? per : 1);
+}
+
+// Pieces of one tile: for every non-empty box, one piece per frame and per
+// run of box_piece_rows() rows.  Boxes are enumerated from the most bands to
+// the fewest, so the longest pieces are dispatched first.
+__host__ __device__ inline int tile_pieces(int ndim, int Kt, int Ky, int Kx, int ebt, int eby, int ebx, int vec,
+                                           int rows_per_thread) {
+    int total = 0;
+    const int nb = ndim == 3 ? 8 : 4;
+    for (int b = nb - 1; b >= 0; --b) {
+        const BoxShape s = box_shape(b, Kt, Ky, Kx, ebt, eby, ebx, vec);
+        if (s.nt <= 0 || s.ny <= 0 || s.width <= 0) continue;
+        const int R = box_piece_rows(b, s.width, rows_per_thread);
+        total += s.nt * ((s.ny + R - 1) / R);
+    }
+    return total;
+}
+
 // Launch configuration picked by the host.
 struct StitchLaunch {
     int ndim;       // 2 or 3
     int dtype;      // Dtype
     int vec;        // elements per chunk: 16 bytes / sizeof(dtype), or 1
-    int kx;         // chunks per thread per virtual row
-    int grid;       // CTAs
-    int block;      // threads per CTA
+    int grid_x;     // planes * tiles (tile fastest)
+    int grid_y;     // pieces per tile (max over tiles)
+    int grid_z;     // 1
+    int smem;       // bytes of coefficient staging
 };
 
 // Implemented in tb_stitch.cu.
 cudaError_t launch_stitch_small(const StitchParamsSmall& p, const StitchLaunch& l, cudaStream_t s);
 cudaError_t launch_stitch_large(const StitchParamsLarge& p, const StitchLaunch& l, cudaStream_t s);
-int stitch_kernel_max_ctas_per_sm(const StitchLaunch& l, bool large);
 
 // ---------------------------------------------------------------------------
 // PatchGroupNorm

@@ -26,19 +26,39 @@
 // The explicit _rn intrinsics (and -fmad=false for this file) keep every
 // product and sum separately rounded, as the rounding contract requires.
 //
-// Data movement.  One thread owns one 16-byte chunk (8 x 16-bit or 4 x fp32
-// elements) per output row, or one element where the geometry is not
-// 16-byte aligned.  Its chunk's column placement -- tile column, band
-// membership, neighbour column -- is fixed for every row it visits, so it is
-// resolved once per thread.  Rows are spread over a persistent grid;
-// everything about a row is uniform across the threads that share it.  Each
-// output element is written once with a 128-bit streaming store, each tile
-// element is read once with a 128-bit streaming load: the kernel moves the
-// algorithmic minimum, all tile bytes plus all output bytes.
+// Data movement.  The kept part of every tile splits into at most 2^d
+// rectangular boxes by band membership (interior, width band, height band,
+// corner; times the time band in 3D).  Inside a box every element needs the
+// same set of source tiles, so one CTA takes one piece of one box (a run of
+// rows of one frame of one (batch, channel) plane) and runs a path compiled
+// for exactly that set: no per-element band tests and no divergence.
+// Threads are laid out 2D over the box: a thread keeps its columns -- and
+// so its width coefficients -- for every row it visits, and each row costs
+// one multiply-add per source address.  Loads of several rows are issued
+// before their arithmetic; 128-bit streaming loads and stores.  Each output
+// element is written once and each tile element read once: the kernel moves
+// the algorithmic minimum, all tile bytes plus all output bytes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "tb_internal.h"
+
+// Rows in flight per thread, by box kind (copy / one band / two bands / three).
+#ifndef TB_STITCH_UR_COPY
+#define TB_STITCH_UR_COPY 4
+#endif
+#ifndef TB_STITCH_UR_ONE
+#define TB_STITCH_UR_ONE 2
+#endif
+#ifndef TB_STITCH_UR_TWO
+#define TB_STITCH_UR_TWO 1
+#endif
+#ifndef TB_STITCH_UR_THREE
+#define TB_STITCH_UR_THREE 1
+#endif
+#ifndef TB_STITCH_MIN_CTAS_2D
+#define TB_STITCH_MIN_CTAS_2D 4
+#endif
 
 namespace tb {
 namespace {
@@ -88,31 +108,34 @@ struct Chunk {
     uint32_t w[WORDS];
 };
 
+// Chunk at element offset `e` of `base` (16-byte aligned when VEC * size is 16).
 template <int DT, int VEC>
-__device__ __forceinline__ Chunk<DT, VEC> load_chunk(const void* base, int64_t chunk_index) {
+__device__ __forceinline__ Chunk<DT, VEC> load_chunk(const void* base, int64_t e) {
     Chunk<DT, VEC> c;
+    const char* p = reinterpret_cast<const char*>(base) + e * Elt<DT>::BYTES;
     if constexpr (VEC * Elt<DT>::BYTES == 16) {
-        uint4 v = __ldcs(reinterpret_cast<const uint4*>(base) + chunk_index);
+        uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
         c.w[0] = v.x;
         c.w[1] = v.y;
         c.w[2] = v.z;
         c.w[3] = v.w;
     } else if constexpr (Elt<DT>::BYTES == 4) {
-        c.w[0] = __ldcs(reinterpret_cast<const unsigned int*>(base) + chunk_index);
+        c.w[0] = __ldcs(reinterpret_cast<const unsigned int*>(p));
     } else {
-        c.w[0] = __ldcs(reinterpret_cast<const unsigned short*>(base) + chunk_index);
+        c.w[0] = __ldcs(reinterpret_cast<const unsigned short*>(p));
     }
     return c;
 }
 
 template <int DT, int VEC>
-__device__ __forceinline__ void store_chunk(void* base, int64_t chunk_index, const Chunk<DT, VEC>& c) {
+__device__ __forceinline__ void store_chunk(void* base, int64_t e, const Chunk<DT, VEC>& c) {
+    char* p = reinterpret_cast<char*>(base) + e * Elt<DT>::BYTES;
     if constexpr (VEC * Elt<DT>::BYTES == 16) {
-        __stcs(reinterpret_cast<uint4*>(base) + chunk_index, make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]));
+        __stcs(reinterpret_cast<uint4*>(p), make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]));
     } else if constexpr (Elt<DT>::BYTES == 4) {
-        __stcs(reinterpret_cast<unsigned int*>(base) + chunk_index, c.w[0]);
+        __stcs(reinterpret_cast<unsigned int*>(p), c.w[0]);
     } else {
-        __stcs(reinterpret_cast<unsigned short*>(base) + chunk_index, (unsigned short)(c.w[0] & 0xffffu));
+        __stcs(reinterpret_cast<unsigned short*>(p), (unsigned short)(c.w[0] & 0xffffu));
     }
 }
 
@@ -178,159 +201,187 @@ __device__ __forceinline__ void eval_nodes(Chunk<DT, VEC> (&F)[NDIM == 3 ? 8 : 4
     }
 }
 
-// Index of the tile whose output range [off[n], off[n+1]) holds v.
-template <int MAXA>
-__device__ __forceinline__ int find_tile(const StitchAxis<MAXA>& a, int v) {
-    int lo = 0, hi = a.n - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.off[mid] <= v)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
+// Per-CTA description of its box piece.
+struct Piece {
+    int64_t plane;       // (batch, channel) plane
+    int k, i, j;         // tile
+    int need;            // box bits: 4 time band, 2 height band, 1 width band
+    int ct;              // frame inside the tile (3D)
+    int rbeg, rend;      // rows [rbeg, rend) inside the tile
+    int x0, width;       // first column (elements) and width (chunks)
+    int bdx, bdy, cpt;   // thread layout
+};
 
-template <int NDIM, int DT, int VEC, int KX, int MAXA, int MAXT, int MAXC>
-__global__ void __launch_bounds__(512) stitch_kernel(const __grid_constant__ StitchParams<MAXA, MAXT, MAXC> p) {
+// One box, compiled for its set of source tiles NEED.  Rows are processed UR
+// at a time: all their loads first, then the arithmetic and the stores.
+template <int NDIM, int NEED, int UR, int DT, int VEC, int MAXA, int MAXT, int MAXC>
+__device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p, const Piece& pc,
+                                        const float* s_xw, const float* s_xu, const float* s_yw, const float* s_yu,
+                                        float wt, float ut) {
     constexpr int NN = NDIM == 3 ? 8 : 4;
     using C = Chunk<DT, VEC>;
-    extern __shared__ float2 s_coef[];
-
-    // coefficient tables into shared memory (lane-varying width coefficients
-    // would serialise on the constant bank)
-    const int ncoef = p.ncoef;
-    for (int q = threadIdx.x; q < ncoef; q += blockDim.x) s_coef[q] = p.coef[q];
-    __syncthreads();
-
     const auto& AT = p.ax[0];
     const auto& AY = p.ax[1];
     const auto& AX = p.ax[2];
-    const int nx = AX.n, ny = AY.n;
-    const int xs = threadIdx.x % p.xt;
-    const int rs = threadIdx.x / p.xt;
-    const uint32_t nseg = (uint32_t)p.nseg, OH = (uint32_t)p.OH, OT = (uint32_t)p.OT;
-    const int64_t OW = p.OW;
-
-    // this thread's chunks in the current row segment
-    int cur_seg = -1;
-    int xj[KX], xcx[KX], xcxn[KX], xcoef[KX], xout[KX];
-    bool xband[KX], xvalid[KX];
-
-    for (int64_t vrow = (int64_t)blockIdx.x * p.rp + rs; vrow < p.nvrows; vrow += (int64_t)gridDim.x * p.rp) {
-        const uint32_t vr = (uint32_t)vrow;
-        const uint32_t seg = vr % nseg;
-        const uint32_t row = vr / nseg;
-        if ((int)seg != cur_seg) {
-            cur_seg = (int)seg;
+    const int tx = threadIdx.x % pc.bdx;
+    const int ty = threadIdx.x / pc.bdx;
+    if (ty >= pc.bdy) return;
+    const int ny = AY.n, nx = AX.n;
+    const int64_t plane = pc.plane;
+    for (int q = 0; q < pc.cpt; ++q) {
+        const int c = tx + q * pc.bdx;
+        if (c >= pc.width) break;
+        const int cx = pc.x0 + c * VEC;
+        float xw[VEC], xu[VEC];
+        if constexpr ((NEED & 1) != 0) {
 #pragma unroll
-            for (int k = 0; k < KX; ++k) {
-                const int x0 = ((int)seg * p.seg_chunks + xs + k * p.xt) * VEC;
-                xvalid[k] = x0 < OW;
-                const int x = xvalid[k] ? x0 : 0;
-                const int j = find_tile(AX, x);
-                const int cx = x - AX.off[j];
-                xj[k] = j;
-                xcx[k] = cx;
-                xout[k] = x;
-                xband[k] = j > 0 && cx < AX.blend[j];
-                xcxn[k] = xband[k] ? AX.ext[j - 1] - AX.blend[j] + cx : 0;
-                xcoef[k] = xband[k] ? AX.coef[j] + cx : 0;
+            for (int l = 0; l < VEC; ++l) {
+                xw[l] = s_xw[cx + l];
+                xu[l] = s_xu[cx + l];
             }
         }
-        // the row: (plane, t, y)
-        const uint32_t y = row % OH;
-        const uint32_t r2 = row / OH;
-        const uint32_t t = NDIM == 3 ? r2 % OT : 0u;
-        const uint32_t plane = NDIM == 3 ? r2 / OT : r2;
-
-        const int i = find_tile(AY, (int)y);
-        const int cy = (int)y - AY.off[i];
-        const bool by = i > 0 && cy < AY.blend[i];
-        const int cyn = by ? AY.ext[i - 1] - AY.blend[i] + cy : 0;
-        float wy = 0.f, uy = 0.f;
-        if (by) {
-            const float2 c = s_coef[AY.coef[i] + cy];
-            wy = c.x;
-            uy = c.y;
+        // per source node: address of its row-0 chunk and its row pitch in bytes
+        const char* nrow0[NN];
+        int32_t npitch[NN];
+#pragma unroll
+        for (int m = 0; m < NN; ++m) {
+            if ((m & ~NEED) != 0) continue;
+            const int dt = (m >> 2) & 1, dy = (m >> 1) & 1, dx = m & 1;
+            const int kq = pc.k - dt, iq = pc.i - dy, jq = pc.j - dx;
+            const int64_t Lt = NDIM == 3 ? AT.ext[kq] : 1;
+            const int64_t Ly = AY.ext[iq];
+            const int64_t Lx = AX.ext[jq];
+            const int lt = NDIM == 3 ? (dt ? AT.ext[pc.k - 1] - AT.blend[pc.k] + pc.ct : pc.ct) : 0;
+            const int ly0 = dy ? AY.ext[pc.i - 1] - AY.blend[pc.i] : 0;
+            const int lx = dx ? AX.ext[pc.j - 1] - AX.blend[pc.j] + cx : cx;
+            nrow0[m] = reinterpret_cast<const char*>(p.tiles[(kq * ny + iq) * nx + jq]) +
+                       (((plane * Lt + lt) * Ly + ly0) * Lx + lx) * Elt<DT>::BYTES;
+            npitch[m] = (int32_t)(Lx * Elt<DT>::BYTES);
         }
-        int kk = 0, ct = 0, ctn = 0;
-        bool bt = false;
-        float wt = 0.f, ut = 0.f;
-        if constexpr (NDIM == 3) {
-            kk = find_tile(AT, (int)t);
-            ct = (int)t - AT.off[kk];
-            bt = kk > 0 && ct < AT.blend[kk];
-            ctn = bt ? AT.ext[kk - 1] - AT.blend[kk] + ct : 0;
-            if (bt) {
-                const float2 c = s_coef[AT.coef[kk] + ct];
-                wt = c.x;
-                ut = c.y;
+        const int64_t OW = p.OW;
+        char* orow0 = reinterpret_cast<char*>(p.out) +
+                      (((plane * p.OT + (NDIM == 3 ? AT.off[pc.k] + pc.ct : 0)) * (int64_t)p.OH + AY.off[pc.i]) * OW +
+                       AX.off[pc.j] + cx) * Elt<DT>::BYTES;
+        const int32_t opitch = (int32_t)(OW * Elt<DT>::BYTES);
+        for (int r = pc.rbeg + ty; r < pc.rend; r += UR * pc.bdy) {
+            C F[UR][NN];
+#pragma unroll
+            for (int u = 0; u < UR; ++u) {
+                const int ru = r + u * pc.bdy;
+                if (ru < pc.rend) {
+#pragma unroll
+                    for (int m = 0; m < NN; ++m) {
+                        if ((m & ~NEED) != 0) continue;
+                        F[u][m] = load_chunk<DT, VEC>(nrow0[m] + (int64_t)ru * npitch[m], 0);
+                    }
+                }
             }
-        }
-        // per (dt, dy) node: tile row index and element offset of the row
-        // start inside that tile, in units of the tile's row length
-        int64_t rbase[2][2];
-        int tbase[2][2];
 #pragma unroll
-        for (int dt = 0; dt < 2; ++dt) {
-#pragma unroll
-            for (int dy = 0; dy < 2; ++dy) {
-                const bool use = (dt == 0 || bt) && (dy == 0 || by) && (NDIM == 3 || dt == 0);
-                const int kq = use ? kk - dt : 0;
-                const int iq = use ? i - dy : 0;
-                const int64_t Lt = NDIM == 3 ? AT.ext[kq] : 1;
-                const int lt = dt ? ctn : ct;
-                const int ly = dy ? cyn : cy;
-                rbase[dt][dy] = ((int64_t)plane * Lt + lt) * AY.ext[iq] + ly;
-                tbase[dt][dy] = (kq * ny + iq) * nx;
-            }
-        }
-        const int64_t obase = (((int64_t)plane * (NDIM == 3 ? OT : 1u) + t) * OH + y) * OW;
-
-        // issue every load of this row before any arithmetic
-        C F[KX][NN];
-        int need[KX];
-#pragma unroll
-        for (int k = 0; k < KX; ++k) {
-            need[k] = (bt ? 4 : 0) | (by ? 2 : 0) | (xband[k] ? 1 : 0);
-            if (!xvalid[k]) need[k] = -1;
-#pragma unroll
-            for (int m = 0; m < NN; ++m) {
-                if (need[k] >= 0 && (m & ~need[k]) == 0) {
-                    const int dt = (m >> 2) & 1, dy = (m >> 1) & 1, dx = m & 1;
-                    const int jq = xj[k] - dx;
-                    const int lx = dx ? xcxn[k] : xcx[k];
-                    const int64_t e = rbase[dt][dy] * AX.ext[jq] + lx;
-                    F[k][m] = load_chunk<DT, VEC>(p.tiles[tbase[dt][dy] + jq], (int64_t)((uint64_t)e / VEC));
+            for (int u = 0; u < UR; ++u) {
+                const int ru = r + u * pc.bdy;
+                if (ru < pc.rend) {
+                    if constexpr (NEED != 0) {
+                        float wy = 0.f, uy = 0.f;
+                        if constexpr ((NEED & 2) != 0) {
+                            wy = s_yw[ru];
+                            uy = s_yu[ru];
+                        }
+                        eval_nodes<NDIM, NEED, DT, VEC>(F[u], wt, ut, wy, uy, [&](int l) { return xw[l]; },
+                                                        [&](int l) { return xu[l]; });
+                    }
+                    store_chunk<DT, VEC>(orow0 + (int64_t)ru * opitch, 0, F[u][0]);
                 }
             }
         }
-#pragma unroll
-        for (int k = 0; k < KX; ++k) {
-            if (need[k] < 0) continue;
-            const int cb = xcoef[k];
-            auto xw = [&](int l) { return s_coef[cb + l].x; };
-            auto xu = [&](int l) { return s_coef[cb + l].y; };
-            switch (need[k]) {
-                case 0: break;
-                case 1: eval_nodes<NDIM, 1, DT, VEC>(F[k], wt, ut, wy, uy, xw, xu); break;
-                case 2: eval_nodes<NDIM, 2, DT, VEC>(F[k], wt, ut, wy, uy, xw, xu); break;
-                case 3: eval_nodes<NDIM, 3, DT, VEC>(F[k], wt, ut, wy, uy, xw, xu); break;
-                default:
-                    if constexpr (NDIM == 3) {
-                        switch (need[k]) {
-                            case 4: eval_nodes<NDIM, 4, DT, VEC>(F[k], wt, ut, wy, uy, xw, xu); break;
-                            case 5: eval_nodes<NDIM, 5, DT, VEC>(F[k], wt, ut, wy, uy, xw, xu); break;
-                            case 6: eval_nodes<NDIM, 6, DT, VEC>(F[k], wt, ut, wy, uy, xw, xu); break;
-                            case 7: eval_nodes<NDIM, 7, DT, VEC>(F[k], wt, ut, wy, uy, xw, xu); break;
-                        }
-                    }
-                    break;
-            }
-            store_chunk<DT, VEC>(p.out, (int64_t)((uint64_t)(obase + xout[k]) / VEC), F[k][0]);
+    }
+}
+
+template <int NDIM, int DT, int VEC, int MAXA, int MAXT, int MAXC>
+__global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? 2 : TB_STITCH_MIN_CTAS_2D)) stitch_kernel(const __grid_constant__ StitchParams<MAXA, MAXT, MAXC> p) {
+    extern __shared__ float s_coef[];
+    const auto& AT = p.ax[0];
+    const auto& AY = p.ax[1];
+    const auto& AX = p.ax[2];
+
+    // which tile, which box, which rows
+    // blockIdx.x runs over (plane, tile) with the tile fastest and
+    // blockIdx.y over the tile's pieces, heaviest first: the GPU dispatches
+    // every tile's longest pieces before any short one.
+    Piece pc;
+    const int ntiles = AX.n * AY.n * (NDIM == 3 ? AT.n : 1);
+    const int tile = (int)(blockIdx.x % (unsigned)ntiles);
+    pc.plane = (int64_t)(blockIdx.x / (unsigned)ntiles);
+    pc.j = tile % AX.n;
+    pc.i = (tile / AX.n) % AY.n;
+    pc.k = NDIM == 3 ? tile / (AX.n * AY.n) : 0;
+    const int Kt = NDIM == 3 ? AT.off[pc.k + 1] - AT.off[pc.k] : 1;
+    const int Ky = AY.off[pc.i + 1] - AY.off[pc.i];
+    const int Kx = AX.off[pc.j + 1] - AX.off[pc.j];
+    const int ebt = (NDIM == 3 && pc.k > 0) ? min(AT.blend[pc.k], Kt) : 0;
+    const int eby = pc.i > 0 ? min(AY.blend[pc.i], Ky) : 0;
+    const int ebx = pc.j > 0 ? min(AX.blend[pc.j], Kx) : 0;
+    int piece = blockIdx.y;
+    pc.need = -1;
+    constexpr int NB = NDIM == 3 ? 8 : 4;
+    for (int b = NB - 1; b >= 0; --b) {  // same order as tile_pieces()
+        const BoxShape s = box_shape(b, Kt, Ky, Kx, ebt, eby, ebx, VEC);
+        if (s.nt <= 0 || s.ny <= 0 || s.width <= 0) continue;
+        const int R = box_piece_rows(b, s.width, p.rows_per_thread);
+        const int nyp = (s.ny + R - 1) / R;
+        if (piece < s.nt * nyp) {
+            pc.need = b;
+            pc.ct = s.t0 + piece / nyp;
+            pc.rbeg = s.y0 + (piece % nyp) * R;
+            pc.rend = min(s.y0 + s.ny, pc.rbeg + R);
+            pc.x0 = s.x0;
+            pc.width = s.width;
+            box_layout(s.width, pc.bdx, pc.bdy, pc.cpt);
+            break;
         }
+        piece -= s.nt * nyp;
+    }
+    if (pc.need < 0) return;  // this tile has fewer pieces than the grid row
+
+    // stage the band coefficients this box needs
+    float* s_xw = s_coef;
+    float* s_xu = s_xw + ebx;
+    float* s_yw = s_xu + ebx;
+    float* s_yu = s_yw + eby;
+    if (pc.need & 1)
+        for (int c = threadIdx.x; c < ebx; c += blockDim.x) {
+            const float2 v = p.coef[AX.coef[pc.j] + c];
+            s_xw[c] = v.x;
+            s_xu[c] = v.y;
+        }
+    if (pc.need & 2)
+        for (int c = threadIdx.x; c < eby; c += blockDim.x) {
+            const float2 v = p.coef[AY.coef[pc.i] + c];
+            s_yw[c] = v.x;
+            s_yu[c] = v.y;
+        }
+    float wt = 0.f, ut = 0.f;
+    if (pc.need & 4) {
+        const float2 v = p.coef[AT.coef[pc.k] + pc.ct];
+        wt = v.x;
+        ut = v.y;
+    }
+    __syncthreads();
+
+    switch (pc.need) {
+        case 0: run_box<NDIM, 0, TB_STITCH_UR_COPY, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+        case 1: run_box<NDIM, 1, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+        case 2: run_box<NDIM, 2, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+        case 3: run_box<NDIM, 3, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+        default:
+            if constexpr (NDIM == 3) {
+                switch (pc.need) {
+                    case 4: run_box<NDIM, 4, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+                    case 5: run_box<NDIM, 5, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+                    case 6: run_box<NDIM, 6, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+                    case 7: run_box<NDIM, 7, TB_STITCH_UR_THREE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+                }
+            }
+            break;
     }
 }
 
@@ -338,36 +389,35 @@ template <int MAXA, int MAXT, int MAXC>
 using KernelFn = void (*)(const StitchParams<MAXA, MAXT, MAXC>);
 
 template <int NDIM, int DT, int MAXA, int MAXT, int MAXC>
-KernelFn<MAXA, MAXT, MAXC> pick_vec(int vec, int kx) {
+KernelFn<MAXA, MAXT, MAXC> pick_vec(int vec) {
     constexpr int V = 16 / Elt<DT>::BYTES;
-    if (vec == 1) {
-        return kx == 2 ? stitch_kernel<NDIM, DT, 1, 2, MAXA, MAXT, MAXC>
-                       : stitch_kernel<NDIM, DT, 1, 1, MAXA, MAXT, MAXC>;
-    }
-    return kx == 2 ? stitch_kernel<NDIM, DT, V, 2, MAXA, MAXT, MAXC> : stitch_kernel<NDIM, DT, V, 1, MAXA, MAXT, MAXC>;
+    return vec == 1 ? stitch_kernel<NDIM, DT, 1, MAXA, MAXT, MAXC> : stitch_kernel<NDIM, DT, V, MAXA, MAXT, MAXC>;
 }
 
 template <int MAXA, int MAXT, int MAXC>
 KernelFn<MAXA, MAXT, MAXC> pick(const StitchLaunch& l) {
     if (l.ndim == 3) {
         switch (l.dtype) {
-            case F32: return pick_vec<3, F32, MAXA, MAXT, MAXC>(l.vec, l.kx);
-            case F16: return pick_vec<3, F16, MAXA, MAXT, MAXC>(l.vec, l.kx);
-            default: return pick_vec<3, BF16, MAXA, MAXT, MAXC>(l.vec, l.kx);
+            case F32: return pick_vec<3, F32, MAXA, MAXT, MAXC>(l.vec);
+            case F16: return pick_vec<3, F16, MAXA, MAXT, MAXC>(l.vec);
+            default: return pick_vec<3, BF16, MAXA, MAXT, MAXC>(l.vec);
         }
     }
     switch (l.dtype) {
-        case F32: return pick_vec<2, F32, MAXA, MAXT, MAXC>(l.vec, l.kx);
-        case F16: return pick_vec<2, F16, MAXA, MAXT, MAXC>(l.vec, l.kx);
-        default: return pick_vec<2, BF16, MAXA, MAXT, MAXC>(l.vec, l.kx);
+        case F32: return pick_vec<2, F32, MAXA, MAXT, MAXC>(l.vec);
+        case F16: return pick_vec<2, F16, MAXA, MAXT, MAXC>(l.vec);
+        default: return pick_vec<2, BF16, MAXA, MAXT, MAXC>(l.vec);
     }
 }
 
 template <int MAXA, int MAXT, int MAXC>
 cudaError_t launch(const StitchParams<MAXA, MAXT, MAXC>& p, const StitchLaunch& l, cudaStream_t s) {
     auto fn = pick<MAXA, MAXT, MAXC>(l);
-    const size_t smem = sizeof(float2) * (size_t)p.ncoef;
-    fn<<<l.grid, l.block, smem, s>>>(p);
+    if (l.smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem);
+        if (e != cudaSuccess) return e;
+    }
+    fn<<<dim3(l.grid_x, l.grid_y, l.grid_z), STITCH_BLOCK, l.smem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -379,23 +429,6 @@ cudaError_t launch_stitch_small(const StitchParamsSmall& p, const StitchLaunch& 
 
 cudaError_t launch_stitch_large(const StitchParamsLarge& p, const StitchLaunch& l, cudaStream_t s) {
     return launch(p, l, s);
-}
-
-int stitch_kernel_max_ctas_per_sm(const StitchLaunch& l, bool large) {
-    int n = 0;
-    cudaError_t e;
-    if (large) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick<LARGE_MAXA, LARGE_MAXT, LARGE_MAXC>(l), l.block,
-                                                          sizeof(float2) * LARGE_MAXC);
-    } else {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick<SMALL_MAXA, SMALL_MAXT, SMALL_MAXC>(l), l.block,
-                                                          sizeof(float2) * SMALL_MAXC);
-    }
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 1;
-    }
-    return n > 0 ? n : 1;
 }
 
 }  // namespace tb
