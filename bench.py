@@ -413,6 +413,47 @@ def per_kernel(torch, tb, W, dev, peak, reps):
     return res
 
 
+def run_profile_target(args):
+    """Launch one kernel on one workload W + K times with plain launches (no
+    graph, no rotation): the command line ncu captures are taken from."""
+    import torch
+    from patch_groupnorm_gb300 import build as lib_build
+    lib_build.build()
+    from patch_groupnorm_gb300 import tileblend as tb
+    from patch_groupnorm_gb300 import workloads as W
+    kernel, _, name = args.profile.partition(":")
+    dev = torch.device("cuda", 0)
+    if kernel in ("stitch2d", "stitch3d"):
+        w = W.STITCH[name]
+        axes = [tb.Axis(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in w.axes]
+        lays = [tb.tb_axis_layout(a) for a in axes]
+        tiles = W.make_stitch_tiles(w, [list(zip(l.origins, l.extents)) for l in lays], [l.out_extent for l in lays])
+        tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+        out = torch.empty((w.B, w.C, *[l.out_extent for l in lays]), dtype=tdt, device=dev)
+        if w.ndim == 2:
+            dt = [[t.to(dev) for t in row] for row in tiles]
+            launch = lambda: tb.tb_stitch2d(dt, axes[0], axes[1], out)
+        else:
+            dt = [[[t.to(dev) for t in row] for row in pl] for pl in tiles]
+            launch = lambda: tb.tb_stitch3d(dt, axes[0], axes[1], axes[2], out)
+    else:
+        w = W.GROUPNORM[name]
+        patches, gamma, beta = W.make_groupnorm_inputs(w)
+        dp = [p.to(dev) for p in patches]
+        outs = [torch.empty_like(p) for p in dp]
+        part = tb.new_partials(len(dp), dp[0].shape[0], w.groups, dev)
+        g, b = gamma.to(dev), beta.to(dev)
+        tb.tb_patch_gn_stats(dp, w.groups, part)
+        if kernel == "gn_stats":
+            launch = lambda: tb.tb_patch_gn_stats(dp, w.groups, part)
+        else:
+            launch = lambda: tb.tb_patch_gn_apply(dp, outs, w.groups, part, g, b, w.eps, True)
+    for _ in range(args.warmup + args.steps):
+        launch()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
+
+
 def cpu_baseline(w, lays_lib, tiles_cpu, alg_bytes):
     """The CPU oracle, as it stands, on one full step of the workload."""
     import numpy as np
@@ -487,9 +528,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kernels", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    help="KERNEL:WORKLOAD (stitch2d|stitch3d|gn_stats|gn_apply): plain launches for ncu")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    if args.profile:
+        run_profile_target(args)
+        return
     if args.impl == "reference":
         if "--steps" not in sys.argv:
             args.steps = 5

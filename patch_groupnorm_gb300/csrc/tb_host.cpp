@@ -212,7 +212,8 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     l.grid_x = (int)(ntiles * planes);
     l.grid_y = max_pieces;
     l.grid_z = 1;
-    l.smem = (int)(sizeof(float) * 2 * (size_t)(max_ebx + max_eby));
+    // vector path: 8 staging slots of 16 bytes per thread, then coefficients
+    l.smem = (vec > 1 ? 8 * tb::STITCH_BLOCK * 16 : 0) + (int)(sizeof(float) * 2 * (size_t)(max_ebx + max_eby));
     if (l.smem > 200 * 1024) return TB_ERR_UNSUPPORTED;
     (void)large;
 

@@ -24,7 +24,8 @@
 // (w, u) = ((float)(c/e), (float)(1 - c/e)) from double quotients, fp32
 // products and sum, and rnd() round-to-nearest-even into the storage type.
 // The explicit _rn intrinsics (and -fmad=false for this file) keep every
-// product and sum separately rounded, as the rounding contract requires.
+// product and sum separately rounded, as the rounding contract requires
+// (see blend() for why the narrow-type sums may use packed adds).
 //
 // Data movement.  The kept part of every tile splits into at most 2^d
 // rectangular boxes by band membership (interior, width band, height band,
@@ -59,6 +60,9 @@
 #ifndef TB_STITCH_MIN_CTAS_2D
 #define TB_STITCH_MIN_CTAS_2D 4
 #endif
+#ifndef TB_STITCH_MIN_CTAS_3D
+#define TB_STITCH_MIN_CTAS_3D 4
+#endif
 
 namespace tb {
 namespace {
@@ -87,6 +91,12 @@ struct Elt<F16> {
         __half2 h = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<const uint32_t*>(&h);
     }
+    // a + b rounded once to fp16, lane by lane
+    __device__ __forceinline__ static uint32_t add2(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
+    }
 };
 template <>
 struct Elt<BF16> {
@@ -98,6 +108,12 @@ struct Elt<BF16> {
     __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    // a + b rounded once to bf16, lane by lane
+    __device__ __forceinline__ static uint32_t add2(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
     }
 };
 
@@ -141,6 +157,12 @@ __device__ __forceinline__ void store_chunk(void* base, int64_t e, const Chunk<D
 
 // blend(P, Q) lane by lane: rnd(rnd(P * u[l]) + rnd(Q * w[l])).
 // Coefficients are read through `cw(l)` / `cu(l)`.
+//
+// For fp16 / bf16 the two rounded products are added with one packed
+// add.rn.{f16,bf16}x2.  That equals the contract's fp32 add followed by
+// rounding: the fp32 sum of two fp16 (bf16) values is exact unless their
+// exponents differ by more than 13 (16); then the smaller one lies far below
+// half an ulp of the larger, and both routes return the larger.
 template <int DT, int VEC, class CW, class CU>
 __device__ __forceinline__ Chunk<DT, VEC> blend(const Chunk<DT, VEC>& P, const Chunk<DT, VEC>& Q, CW cw, CU cu) {
     Chunk<DT, VEC> R;
@@ -152,12 +174,12 @@ __device__ __forceinline__ Chunk<DT, VEC> blend(const Chunk<DT, VEC>& P, const C
             R.w[q] = __float_as_uint(__fadd_rn(pa, qb));
         }
     } else if constexpr (VEC == 1) {
-        float a, b, ra, rb, dummy;
+        float a, b, dummy;
         Elt<DT>::unpack(P.w[0], a, dummy);
         Elt<DT>::unpack(Q.w[0], b, dummy);
-        Elt<DT>::unpack(Elt<DT>::pack(__fmul_rn(a, cu(0)), 0.f), ra, dummy);
-        Elt<DT>::unpack(Elt<DT>::pack(__fmul_rn(b, cw(0)), 0.f), rb, dummy);
-        R.w[0] = Elt<DT>::pack(__fadd_rn(ra, rb), 0.f) & 0xffffu;
+        const uint32_t pa = Elt<DT>::pack(__fmul_rn(a, cu(0)), 0.f);
+        const uint32_t qb = Elt<DT>::pack(__fmul_rn(b, cw(0)), 0.f);
+        R.w[0] = Elt<DT>::add2(pa, qb) & 0xffffu;
     } else {
 #pragma unroll
         for (int q = 0; q < Chunk<DT, VEC>::WORDS; ++q) {
@@ -166,10 +188,7 @@ __device__ __forceinline__ Chunk<DT, VEC> blend(const Chunk<DT, VEC>& P, const C
             Elt<DT>::unpack(Q.w[q], b0, b1);
             const uint32_t pa = Elt<DT>::pack(__fmul_rn(a0, cu(2 * q)), __fmul_rn(a1, cu(2 * q + 1)));
             const uint32_t qb = Elt<DT>::pack(__fmul_rn(b0, cw(2 * q)), __fmul_rn(b1, cw(2 * q + 1)));
-            float ra0, ra1, rb0, rb1;
-            Elt<DT>::unpack(pa, ra0, ra1);
-            Elt<DT>::unpack(qb, rb0, rb1);
-            R.w[q] = Elt<DT>::pack(__fadd_rn(ra0, rb0), __fadd_rn(ra1, rb1));
+            R.w[q] = Elt<DT>::add2(pa, qb);
         }
     }
     return R;
@@ -296,9 +315,185 @@ __device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p,
     }
 }
 
+// ---------------------------------------------------------------------------
+// 16-byte path: a per-thread cp.async pipeline through shared memory
+// ---------------------------------------------------------------------------
+
+// Staging slots per thread (16 bytes each): rows in flight x source nodes.
+constexpr int STITCH_SLOTS = 8;
+
+__host__ __device__ constexpr int nodes_of(int need) { return 1 << popc3(need); }
+__host__ __device__ constexpr int stages_of(int need) {
+    return STITCH_SLOTS / nodes_of(need) >= 2 ? STITCH_SLOTS / nodes_of(need) : 1;
+}
+// Position of node m among the nodes of NEED (masks that are subsets of NEED,
+// in increasing order).
+__host__ __device__ constexpr int node_rank(int need, int m) {
+    int r = 0;
+    for (int x = 0; x < m; ++x)
+        if ((x & ~need) == 0) ++r;
+    return r;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gptr) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+template <int DT, int VEC>
+__device__ __forceinline__ Chunk<DT, VEC> lds_chunk(uint32_t saddr) {
+    Chunk<DT, VEC> c;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(c.w[0]), "=r"(c.w[1]), "=r"(c.w[2]), "=r"(c.w[3])
+                 : "r"(saddr));
+    return c;
+}
+
+// Final value of node m (and, recursively, of the nodes it blends with) for
+// the row held in `stage`: the raw value comes from the thread's staging
+// slot right before it is used, which keeps the set of live values small.
+template <int NDIM, int NEED, int M, int DT, int VEC>
+struct NodeEval {
+    template <class Ctx>
+    __device__ __forceinline__ static void run(Ctx& ctx, Chunk<DT, VEC> (&F)[NDIM == 3 ? 8 : 4]) {
+        Chunk<DT, VEC> cur = lds_chunk<DT, VEC>(ctx.slot(node_rank(NEED, M)));
+        if constexpr (NDIM == 3 && (NEED & 4) && !(M & 4))
+            cur = blend<DT, VEC>(F[M | 4], cur, [&](int) { return ctx.wt; }, [&](int) { return ctx.ut; });
+        if constexpr ((NEED & 2) && !(M & 2))
+            cur = blend<DT, VEC>(F[M | 2], cur, [&](int) { return ctx.wy; }, [&](int) { return ctx.uy; });
+        if constexpr ((NEED & 1) && !(M & 1))
+            cur = blend<DT, VEC>(F[M | 1], cur, [&](int l) { return ctx.xw[l]; }, [&](int l) { return ctx.xu[l]; });
+        F[M] = cur;
+    }
+};
+
+template <int NDIM, int NEED, int PC, int M, int DT, int VEC>
+struct PassEval {  // nodes of popcount PC, from mask M downwards
+    template <class Ctx>
+    __device__ __forceinline__ static void run(Ctx& ctx, Chunk<DT, VEC> (&F)[NDIM == 3 ? 8 : 4]) {
+        if constexpr (M >= 0) {
+            if constexpr ((M & ~NEED) == 0 && popc3(M) == PC) NodeEval<NDIM, NEED, M, DT, VEC>::run(ctx, F);
+            PassEval<NDIM, NEED, PC, M - 1, DT, VEC>::run(ctx, F);
+        }
+    }
+};
+
+template <int NDIM, int NEED, int PC, int DT, int VEC>
+struct DagEval {  // popcount PC down to 0
+    template <class Ctx>
+    __device__ __forceinline__ static void run(Ctx& ctx, Chunk<DT, VEC> (&F)[NDIM == 3 ? 8 : 4]) {
+        if constexpr (PC >= 0) {
+            PassEval<NDIM, NEED, PC, (NDIM == 3 ? 7 : 3), DT, VEC>::run(ctx, F);
+            DagEval<NDIM, NEED, PC - 1, DT, VEC>::run(ctx, F);
+        }
+    }
+};
+
+template <int VEC>
+struct RowCtx {
+    uint32_t base;      // this thread's slot 0 of the current stage
+    uint32_t stride;    // bytes between a thread's consecutive slots
+    float wt, ut, wy, uy;
+    float xw[VEC], xu[VEC];
+    __device__ __forceinline__ uint32_t slot(int rank) const { return base + (uint32_t)rank * stride; }
+};
+
+template <int NDIM, int NEED, int DT, int VEC, int MAXA, int MAXT, int MAXC>
+__device__ __forceinline__ void run_box_pipe(const StitchParams<MAXA, MAXT, MAXC>& p, const Piece& pc,
+                                             const float* s_xw, const float* s_xu, const float* s_yw,
+                                             const float* s_yu, float wt, float ut, uint32_t s_slots) {
+    constexpr int NN = NDIM == 3 ? 8 : 4;
+    constexpr int NU = nodes_of(NEED);
+    constexpr int S = stages_of(NEED);
+    using C = Chunk<DT, VEC>;
+    const auto& AT = p.ax[0];
+    const auto& AY = p.ax[1];
+    const auto& AX = p.ax[2];
+    const int tx = threadIdx.x % pc.bdx;
+    const int ty = threadIdx.x / pc.bdx;
+    if (ty >= pc.bdy) return;
+    const int ny = AY.n, nx = AX.n;
+    // slot (stage st, node rank n) of this thread: [st][n][thread] x 16 bytes,
+    // so a warp's 16-byte accesses to one slot are contiguous
+    const uint32_t slot_stride = (uint32_t)STITCH_BLOCK * 16u;
+    const uint32_t my_slot0 = s_slots + (uint32_t)threadIdx.x * 16u;
+    const int64_t plane = pc.plane;
+    RowCtx<VEC> ctx;
+    ctx.stride = slot_stride;
+    ctx.wt = wt;
+    ctx.ut = ut;
+    for (int q = 0; q < pc.cpt; ++q) {
+        const int c = tx + q * pc.bdx;
+        if (c >= pc.width) break;
+        const int cx = pc.x0 + c * VEC;
+        if constexpr ((NEED & 1) != 0) {
+#pragma unroll
+            for (int l = 0; l < VEC; ++l) {
+                ctx.xw[l] = s_xw[cx + l];
+                ctx.xu[l] = s_xu[cx + l];
+            }
+        }
+        const char* nrow0[NU];
+        int32_t npitch[NU];
+#pragma unroll
+        for (int m = 0; m < NN; ++m) {
+            if ((m & ~NEED) != 0) continue;
+            const int dt = (m >> 2) & 1, dy = (m >> 1) & 1, dx = m & 1;
+            const int kq = pc.k - dt, iq = pc.i - dy, jq = pc.j - dx;
+            const int64_t Lt = NDIM == 3 ? AT.ext[kq] : 1;
+            const int64_t Ly = AY.ext[iq];
+            const int64_t Lx = AX.ext[jq];
+            const int lt = NDIM == 3 ? (dt ? AT.ext[pc.k - 1] - AT.blend[pc.k] + pc.ct : pc.ct) : 0;
+            const int ly0 = dy ? AY.ext[pc.i - 1] - AY.blend[pc.i] : 0;
+            const int lx = dx ? AX.ext[pc.j - 1] - AX.blend[pc.j] + cx : cx;
+            nrow0[node_rank(NEED, m)] = reinterpret_cast<const char*>(p.tiles[(kq * ny + iq) * nx + jq]) +
+                                        (((plane * Lt + lt) * Ly + ly0) * Lx + lx) * Elt<DT>::BYTES;
+            npitch[node_rank(NEED, m)] = (int32_t)(Lx * Elt<DT>::BYTES);
+        }
+        const int64_t OW = p.OW;
+        char* orow0 = reinterpret_cast<char*>(p.out) +
+                      (((plane * p.OT + (NDIM == 3 ? AT.off[pc.k] + pc.ct : 0)) * (int64_t)p.OH + AY.off[pc.i]) * OW +
+                       AX.off[pc.j] + cx) * Elt<DT>::BYTES;
+        const int32_t opitch = (int32_t)(OW * Elt<DT>::BYTES);
+
+        const int r0 = pc.rbeg + ty;
+        const int nrows = r0 < pc.rend ? (pc.rend - r0 + pc.bdy - 1) / pc.bdy : 0;
+        auto issue = [&](int m) {  // rows r0 + m * bdy into stage m % S
+            const int row = r0 + m * pc.bdy;
+            const uint32_t st = my_slot0 + (uint32_t)((m % S) * NU) * slot_stride;
+#pragma unroll
+            for (int n = 0; n < NU; ++n) cp_async16(st + (uint32_t)n * slot_stride, nrow0[n] + (int64_t)row * npitch[n]);
+        };
+#pragma unroll
+        for (int m = 0; m < S - 1; ++m) {
+            if (m < nrows) issue(m);
+            cp_async_commit();
+        }
+        for (int m = 0; m < nrows; ++m) {
+            if (m + S - 1 < nrows) issue(m + S - 1);
+            cp_async_commit();
+            cp_async_wait<S - 1>();
+            const int row = r0 + m * pc.bdy;
+            ctx.base = my_slot0 + (uint32_t)((m % S) * NU) * slot_stride;
+            if constexpr ((NEED & 2) != 0) {
+                ctx.wy = s_yw[row];
+                ctx.uy = s_yu[row];
+            }
+            C F[NN];
+            DagEval<NDIM, NEED, 3, DT, VEC>::run(ctx, F);
+            store_chunk<DT, VEC>(orow0 + (int64_t)row * opitch, 0, F[0]);
+        }
+        cp_async_wait<0>();
+    }
+}
+
 template <int NDIM, int DT, int VEC, int MAXA, int MAXT, int MAXC>
-__global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? 2 : TB_STITCH_MIN_CTAS_2D)) stitch_kernel(const __grid_constant__ StitchParams<MAXA, MAXT, MAXC> p) {
-    extern __shared__ float s_coef[];
+__global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_3D : TB_STITCH_MIN_CTAS_2D)) stitch_kernel(const __grid_constant__ StitchParams<MAXA, MAXT, MAXC> p) {
+    extern __shared__ __align__(16) unsigned char s_dyn[];
     const auto& AT = p.ax[0];
     const auto& AY = p.ax[1];
     const auto& AX = p.ax[2];
@@ -342,7 +537,9 @@ __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? 2 : TB_STITCH_MIN_C
     }
     if (pc.need < 0) return;  // this tile has fewer pieces than the grid row
 
-    // stage the band coefficients this box needs
+    // shared memory: the vector path's staging slots, then band coefficients
+    unsigned char* s_stage = s_dyn;
+    float* s_coef = reinterpret_cast<float*>(s_dyn + (VEC * Elt<DT>::BYTES == 16 ? STITCH_SLOTS * STITCH_BLOCK * 16 : 0));
     float* s_xw = s_coef;
     float* s_xu = s_xw + ebx;
     float* s_yw = s_xu + ebx;
@@ -367,21 +564,41 @@ __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? 2 : TB_STITCH_MIN_C
     }
     __syncthreads();
 
-    switch (pc.need) {
-        case 0: run_box<NDIM, 0, TB_STITCH_UR_COPY, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-        case 1: run_box<NDIM, 1, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-        case 2: run_box<NDIM, 2, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-        case 3: run_box<NDIM, 3, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-        default:
-            if constexpr (NDIM == 3) {
-                switch (pc.need) {
-                    case 4: run_box<NDIM, 4, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-                    case 5: run_box<NDIM, 5, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-                    case 6: run_box<NDIM, 6, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-                    case 7: run_box<NDIM, 7, TB_STITCH_UR_THREE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+    if constexpr (VEC * Elt<DT>::BYTES == 16) {
+        const uint32_t s_slots = (uint32_t)__cvta_generic_to_shared(s_stage);
+        switch (pc.need) {
+            case 0: run_box_pipe<NDIM, 0, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+            case 1: run_box_pipe<NDIM, 1, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+            case 2: run_box_pipe<NDIM, 2, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+            case 3: run_box_pipe<NDIM, 3, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+            default:
+                if constexpr (NDIM == 3) {
+                    switch (pc.need) {
+                        case 4: run_box_pipe<NDIM, 4, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+                        case 5: run_box_pipe<NDIM, 5, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+                        case 6: run_box_pipe<NDIM, 6, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+                        case 7: run_box_pipe<NDIM, 7, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+                    }
                 }
-            }
-            break;
+                break;
+        }
+    } else {
+        switch (pc.need) {
+            case 0: run_box<NDIM, 0, TB_STITCH_UR_COPY, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+            case 1: run_box<NDIM, 1, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+            case 2: run_box<NDIM, 2, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+            case 3: run_box<NDIM, 3, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+            default:
+                if constexpr (NDIM == 3) {
+                    switch (pc.need) {
+                        case 4: run_box<NDIM, 4, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+                        case 5: run_box<NDIM, 5, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+                        case 6: run_box<NDIM, 6, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+                        case 7: run_box<NDIM, 7, TB_STITCH_UR_THREE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+                    }
+                }
+                break;
+        }
     }
 }
 
