@@ -18,12 +18,13 @@
 //     n = nA + nB,  d = meanB - meanA,
 //     mean = meanA + d * nB / n,  M2 = M2A + M2B + d^2 * nA * nB / n.
 //
-// gn_stats_kernel: one thread-block cluster per (patch, sample, group).  Each
-// thread runs Welford over blocks of 16 elements (block mean and M2 computed
-// directly, then merged), warps merge with shuffles, warps within a CTA
-// through shared memory, and the CTAs of the cluster through distributed
-// shared memory, in a fixed order (deterministic results).  Reads are 128-bit
-// streaming loads.
+// gn_stats_kernel: one thread-block cluster per (patch, sample, group), sized
+// so the grid is about one wave.  Each thread keeps eight 128-bit streaming
+// loads in flight and folds each batch (64 bf16 / fp16 or 32 fp32 elements)
+// into its running triple with Chan's update after computing the batch's own
+// mean and M2 directly; warps merge with shuffles, warps within a CTA through
+// shared memory, and the CTAs of the cluster through distributed shared
+// memory, in a fixed order (deterministic results).
 //
 // gn_apply_kernel: one CTA per segment of one channel row.  Every warp
 // combines the P partials of its group (lane q holds patch q), forms
@@ -41,6 +42,7 @@ namespace tb {
 namespace {
 
 constexpr int STATS_BLOCK = 256;
+constexpr int STATS_SLOTS = 8;  // cp.async ring slots per thread (16 bytes each)
 constexpr int APPLY_BLOCK = 128;
 constexpr int APPLY_CPT = 4;  // 16-byte chunks per thread per segment
 
@@ -147,54 +149,84 @@ __device__ __forceinline__ Stat warp_reduce(Stat s) {
     return s;  // valid in lane 0
 }
 
+// Chan's update with an approximate quotient, for a thread's own running
+// merge of equal-sized blocks (the counts are exact; the ratio's last-bit
+// error is far below the statistics' tolerance).
+__device__ __forceinline__ Stat chan_fast(const Stat& a, const Stat& b) {
+    const float n = a.n + b.n;
+    const float r = __fdividef(b.n, n);
+    const float d = b.mean - a.mean;
+    Stat s;
+    s.n = n;
+    s.mean = fmaf(d, r, a.mean);
+    s.m2 = a.m2 + b.m2 + d * d * a.n * r;
+    return s;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gptr) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds16(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    return v;
+}
+
 template <int DT, bool VECTOR>
 __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_constant__ GnStatsParams p) {
     constexpr int VEC = 16 / GElt<DT>::BYTES;
+    extern __shared__ __align__(16) unsigned char s_ring[];  // STATS_SLOTS x STATS_BLOCK x 16 bytes
     __shared__ Stat s_warp[STATS_BLOCK / 32];
     __shared__ Stat s_cta;
 
     cg::cluster_group cluster = cg::this_cluster();
-    const int cs = p.cs;
-    const int64_t unit = blockIdx.x / cs;
+    const unsigned cs = (unsigned)p.cs;
+    const unsigned unit = blockIdx.x / cs;
     const int rank = (int)cluster.block_rank();
-    const int64_t NG = p.N * p.G;
-    const int pp = (int)(unit / NG);
-    const int64_t rem = unit - (int64_t)pp * NG;
-    const int64_t n = rem / p.G;
-    const int64_t g = rem - n * p.G;
+    const unsigned NG = (unsigned)p.N * (unsigned)p.G;
+    const unsigned pp = unit / NG;
+    const unsigned rem = unit - pp * NG;
+    const unsigned n = rem / (unsigned)p.G;
+    const unsigned g = rem - n * (unsigned)p.G;
     const int64_t S = p.spatial[pp];
     const int64_t cg_ = p.C / p.G;
     const int64_t len = cg_ * S;
-    const int64_t start = (n * p.C + g * cg_) * S;
+    const int64_t start = ((int64_t)n * p.C + (int64_t)g * cg_) * S;
     const char* base = reinterpret_cast<const char*>(p.patches[pp]) + start * GElt<DT>::BYTES;
 
     Stat acc{0.f, 0.f, 0.f};
     if constexpr (VECTOR) {
-        // len and start are multiples of VEC: whole 16-byte chunks
+        // len and start are multiples of VEC: whole 16-byte chunks.  Each
+        // thread streams its chunks through its own ring of STATS_SLOTS
+        // shared-memory slots with cp.async, STATS_SLOTS - 1 chunks ahead.
         const int64_t nv = len / VEC;
         const int64_t v0 = nv * rank / cs, v1 = nv * (rank + 1) / cs;
         const uint4* src = reinterpret_cast<const uint4*>(base);
-        int64_t v = v0 + threadIdx.x;
-        // two chunks per step: 2 x 16-byte loads in flight, one 2*VEC-element merge
-        for (; v + STATS_BLOCK < v1; v += 2 * STATS_BLOCK) {
-            const uint4 a = __ldcs(src + v);
-            const uint4 b = __ldcs(src + v + STATS_BLOCK);
-            float x[2 * VEC];
-            float xa[VEC], xb[VEC];
-            chunk_to_floats<DT>(a, xa);
-            chunk_to_floats<DT>(b, xb);
+        const int64_t first = v0 + threadIdx.x;
+        const int cnt = first < v1 ? (int)((v1 - first + STATS_BLOCK - 1) / STATS_BLOCK) : 0;
+        const uint32_t ring = (uint32_t)__cvta_generic_to_shared(s_ring) + threadIdx.x * 16u;
+        constexpr uint32_t SLOT = STATS_BLOCK * 16u;
 #pragma unroll
-            for (int q = 0; q < VEC; ++q) {
-                x[q] = xa[q];
-                x[VEC + q] = xb[q];
-            }
-            acc = chan(acc, block_stat<2 * VEC>(x));
+        for (int k = 0; k < STATS_SLOTS - 1; ++k) {
+            if (k < cnt) cp_async16(ring + k * SLOT, src + first + (int64_t)k * STATS_BLOCK);
+            cp_async_commit();
         }
-        if (v < v1) {
+        for (int k = 0; k < cnt; ++k) {
+            const int ahead = k + STATS_SLOTS - 1;
+            if (ahead < cnt)
+                cp_async16(ring + (ahead % STATS_SLOTS) * SLOT, src + first + (int64_t)ahead * STATS_BLOCK);
+            cp_async_commit();
+            cp_async_wait<STATS_SLOTS - 1>();
             float x[VEC];
-            chunk_to_floats<DT>(__ldcs(src + v), x);
-            acc = chan(acc, block_stat<VEC>(x));
+            chunk_to_floats<DT>(lds16(ring + (k % STATS_SLOTS) * SLOT), x);
+            acc = k == 0 ? block_stat<VEC>(x) : chan_fast(acc, block_stat<VEC>(x));
         }
+        cp_async_wait<0>();
     } else {
         const int64_t e0 = len * rank / cs, e1 = len * (rank + 1) / cs;
         for (int64_t e = e0 + threadIdx.x; e < e1; e += STATS_BLOCK) {
@@ -217,7 +249,7 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
     cluster.sync();
     if (rank == 0 && threadIdx.x == 0) {
         Stat t = s_cta;
-        for (int r = 1; r < cs; ++r) t = chan(t, *cluster.map_shared_rank(&s_cta, r));
+        for (int r = 1; r < (int)cs; ++r) t = chan(t, *cluster.map_shared_rank(&s_cta, r));
         GnPartial out;
         out.n = len;
         out.mean = len > 0 ? t.mean : 0.f;
@@ -258,11 +290,27 @@ __device__ __forceinline__ float load_param(const void* ptr, int64_t c, float df
     }
 }
 
+// silu(z) = z / (1 + e^-z), with e^-z = 2^(-z log2 e) and the reciprocal
+// from the approximate special-function unit (relative errors ~2^-22, far
+// inside the output tolerances).  Flushing subnormals there is harmless:
+// e^-z is subnormal only for z > 87, where 1 + e^-z rounds to 1, and the
+// reciprocal only for z < -87, where silu(z) lies below 1e-35.
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <int SILU>
 __device__ __forceinline__ float act(float x, float a, float b) {
     const float z = fmaf(x, a, b);
     if constexpr (SILU) {
-        return __fdividef(z, 1.0f + __expf(-z));
+        return z * rcp_ftz(1.0f + ex2_ftz(z * -1.4426950408889634f));
     } else {
         return z;
     }
@@ -274,17 +322,19 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
     const int64_t item = blockIdx.x;
     int pp = 0;
     while (pp + 1 < p.P && p.item_start[pp + 1] <= item) ++pp;
-    const int64_t local = item - p.item_start[pp];
-    const int64_t nseg = p.nseg[pp];
-    const int64_t row = local / nseg;  // n * C + c
+    // item counts, rows and channels fit 32 bits (the host checks the grid)
+    const unsigned local = (unsigned)(item - p.item_start[pp]);
+    const unsigned nseg = (unsigned)p.nseg[pp];
+    const unsigned row = local / nseg;  // n * C + c
     const int64_t seg = local - row * nseg;
     const int64_t S = p.spatial[pp];
-    const int64_t c = row % p.C;
-    const int64_t n = row / p.C;
-    const int64_t g = c / (p.C / p.G);
+    const unsigned C32 = (unsigned)p.C;
+    const int64_t c = row % C32;
+    const int64_t n = row / C32;
+    const int64_t g = (unsigned)c / (C32 / (unsigned)p.G);
     const int64_t e_begin = seg * p.seg;
     const int64_t e_end = min(S, e_begin + p.seg);
-    const int64_t row_start = row * S;
+    const int64_t row_start = (int64_t)row * S;
 
     if constexpr (VECTOR) {
         // S and every row start are multiples of VEC; issue the data loads first
@@ -343,8 +393,15 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
 }
 
 template <int DT>
+void (*stats_fn(bool aligned))(const GnStatsParams) {
+    return aligned ? gn_stats_kernel<DT, true> : gn_stats_kernel<DT, false>;
+}
+
+size_t stats_smem(bool aligned) { return aligned ? (size_t)STATS_SLOTS * STATS_BLOCK * 16 : 0; }
+
+template <int DT>
 cudaError_t stats_dt(const GnStatsParams& p, int64_t units, cudaStream_t s) {
-    void (*fn)(const GnStatsParams) = p.aligned ? gn_stats_kernel<DT, true> : gn_stats_kernel<DT, false>;
+    void (*fn)(const GnStatsParams) = stats_fn<DT>(p.aligned != 0);
     if (p.cs > 8) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -352,7 +409,7 @@ cudaError_t stats_dt(const GnStatsParams& p, int64_t units, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units * p.cs), 1, 1);
     cfg.blockDim = dim3(STATS_BLOCK, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = stats_smem(p.aligned != 0);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -381,6 +438,21 @@ cudaError_t apply_dt(const GnApplyParams& p, int64_t items, cudaStream_t s) {
 int gn_apply_segment(int dtype, bool aligned) {
     const int bytes = dtype == F32 ? 4 : 2;
     return APPLY_BLOCK * (aligned ? APPLY_CPT * (16 / bytes) : APPLY_CPT);
+}
+
+int gn_stats_ctas_per_sm(int dtype, bool aligned) {
+    void (*fn)(const GnStatsParams);
+    switch (dtype) {
+        case F32: fn = stats_fn<F32>(aligned); break;
+        case F16: fn = stats_fn<F16>(aligned); break;
+        default: fn = stats_fn<BF16>(aligned); break;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, STATS_BLOCK, stats_smem(aligned)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    return n > 0 ? n : 1;
 }
 
 cudaError_t launch_gn_stats(const GnStatsParams& p, int dtype, int64_t units, cudaStream_t s) {

@@ -122,6 +122,19 @@ tb_status device_sms(int* sms) {
     return TB_OK;
 }
 
+// statistics-kernel occupancy per (device, dtype, path), cached
+int g_stats_occ[MAX_DEVICES][3][2] = {};
+
+int gn_stats_occupancy(int dtype, bool aligned) {
+    int dev = 0;
+    (void)cudaGetDevice(&dev);
+    if (dev < 0 || dev >= MAX_DEVICES) return tb::gn_stats_ctas_per_sm(dtype, aligned);
+    std::lock_guard<std::mutex> lock(g_mu);
+    int& v = g_stats_occ[dev][dtype][aligned ? 1 : 0];
+    if (v == 0) v = tb::gn_stats_ctas_per_sm(dtype, aligned);
+    return v;
+}
+
 int elem_bytes(tb_dtype d) { return d == TB_F32 ? 4 : 2; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -188,12 +201,12 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     for (int q = 0; ok && q < ntiles; ++q) ok = aligned16(tiles[q]);
     if (!ok) vec = 1;
 
-    prm.rows_per_thread = TB_STITCH_ROWS_PER_THREAD;
     tb::StitchLaunch l{};
     l.ndim = ndim;
     l.dtype = (int)dtype;
     l.vec = vec;
-    // pieces per tile: the grid's x extent is the largest
+    // Pieces per tile; the grid's second extent is the largest count.
+    const int rpt = TB_STITCH_ROWS_PER_THREAD;
     int max_pieces = 0, max_ebx = 0, max_eby = 0;
     for (int k = 0; k < g[0].n; ++k)
         for (int i = 0; i < g[1].n; ++i)
@@ -203,10 +216,10 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
                 const int ebx = j > 0 ? std::min(g[2].blend[j], g[2].kept[j]) : 0;
                 max_ebx = std::max(max_ebx, ebx);
                 max_eby = std::max(max_eby, eby);
-                const int np = tb::tile_pieces(ndim, g[0].kept[k], g[1].kept[i], g[2].kept[j], ebt, eby, ebx, vec,
-                                               prm.rows_per_thread);
-                max_pieces = std::max(max_pieces, np);
+                max_pieces = std::max(max_pieces, tb::tile_pieces(ndim, g[0].kept[k], g[1].kept[i], g[2].kept[j],
+                                                                  ebt, eby, ebx, vec, rpt));
             }
+    prm.rows_per_thread = rpt;
     if (max_pieces == 0) return TB_OK;
     if ((int64_t)ntiles * planes > 2147483647LL || max_pieces > 65535) return TB_ERR_UNSUPPORTED;
     l.grid_x = (int)(ntiles * planes);
@@ -379,14 +392,17 @@ TB_API tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dty
     prm.P = P;
     prm.G = G;
     prm.aligned = aligned ? 1 : 0;
-    // CTAs per unit: enough to fill the GPU about twice, each with >= 32 KB
+    // CTAs per unit (the cluster size, 1..8): as many as keep the whole grid
+    // within one wave of resident CTAs, each streaming >= 16 KB
     int sms = 0;
     s = device_sms(&sms);
     if (s != TB_OK) return s;
     const int64_t units = (int64_t)P * N * G;
     const int64_t bytes = max_len * elem_bytes(dtype);
-    int cs = 1;
-    while (cs < 16 && units * cs < 2LL * sms * 4 && bytes / (cs * 2) >= 32768) cs *= 2;
+    const int64_t slots = (int64_t)sms * gn_stats_occupancy((int)dtype, aligned);
+    int64_t cs64 = units > 0 ? slots / units : 1;
+    cs64 = std::min<int64_t>(cs64, bytes / 16384);
+    const int cs = (int)std::max<int64_t>(1, std::min<int64_t>(8, cs64));
     prm.cs = cs;
     if (units * cs > 2147483647LL) return TB_ERR_UNSUPPORTED;
     cudaError_t e = tb::launch_gn_stats(prm, (int)dtype, units, reinterpret_cast<cudaStream_t>(stream));

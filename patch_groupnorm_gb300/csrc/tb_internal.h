@@ -167,6 +167,9 @@ int gn_apply_segment(int dtype, bool aligned);
 // Records a CUDA error for tb_last_cuda_error() (defined in tb_host.cpp).
 void record_cuda_error(cudaError_t e);
 
+// Resident statistics CTAs per SM (occupancy of the kernel variant).
+int gn_stats_ctas_per_sm(int dtype, bool aligned);
+
 cudaError_t launch_gn_stats(const GnStatsParams& p, int dtype, int64_t units, cudaStream_t s);
 cudaError_t launch_gn_apply(const GnApplyParams& p, int dtype, int64_t items, cudaStream_t s);
 

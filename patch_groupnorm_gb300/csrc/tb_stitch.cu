@@ -155,6 +155,18 @@ __device__ __forceinline__ void store_chunk(void* base, int64_t e, const Chunk<D
     }
 }
 
+// Two IEEE fp32 products, round-to-nearest, in one packed instruction
+// (per lane identical to __fmul_rn).
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %5};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // blend(P, Q) lane by lane: rnd(rnd(P * u[l]) + rnd(Q * w[l])).
 // Coefficients are read through `cw(l)` / `cu(l)`.
 //
@@ -167,6 +179,8 @@ template <int DT, int VEC, class CW, class CU>
 __device__ __forceinline__ Chunk<DT, VEC> blend(const Chunk<DT, VEC>& P, const Chunk<DT, VEC>& Q, CW cw, CU cu) {
     Chunk<DT, VEC> R;
     if constexpr (Elt<DT>::BYTES == 4) {
+        // fp32: scalar products and sum (a packed product feeding a packed
+        // add could be fused into one rounding)
 #pragma unroll
         for (int q = 0; q < Chunk<DT, VEC>::WORDS; ++q) {
             const float pa = __fmul_rn(__uint_as_float(P.w[q]), cu(q));
@@ -183,12 +197,12 @@ __device__ __forceinline__ Chunk<DT, VEC> blend(const Chunk<DT, VEC>& P, const C
     } else {
 #pragma unroll
         for (int q = 0; q < Chunk<DT, VEC>::WORDS; ++q) {
-            float a0, a1, b0, b1;
+            float a0, a1, b0, b1, pa0, pa1, qb0, qb1;
             Elt<DT>::unpack(P.w[q], a0, a1);
             Elt<DT>::unpack(Q.w[q], b0, b1);
-            const uint32_t pa = Elt<DT>::pack(__fmul_rn(a0, cu(2 * q)), __fmul_rn(a1, cu(2 * q + 1)));
-            const uint32_t qb = Elt<DT>::pack(__fmul_rn(b0, cw(2 * q)), __fmul_rn(b1, cw(2 * q + 1)));
-            R.w[q] = Elt<DT>::add2(pa, qb);
+            mul2_rn(a0, a1, cu(2 * q), cu(2 * q + 1), pa0, pa1);
+            mul2_rn(b0, b1, cw(2 * q), cw(2 * q + 1), qb0, qb1);
+            R.w[q] = Elt<DT>::add2(Elt<DT>::pack(pa0, pa1), Elt<DT>::pack(qb0, qb1));
         }
     }
     return R;
