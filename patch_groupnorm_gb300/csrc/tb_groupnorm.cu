@@ -19,7 +19,7 @@
 //     mean = meanA + d * nB / n,  M2 = M2A + M2B + d^2 * nA * nB / n.
 //
 // gn_stats_kernel: one thread-block cluster per (patch, sample, group), sized
-// so the grid is about one wave.  Each thread keeps eight 128-bit streaming
+// to about two CTAs per SM in all.  Each thread keeps eight 128-bit streaming
 // loads in flight and folds each batch (64 bf16 / fp16 or 32 fp32 elements)
 // into its running triple with Chan's update after computing the batch's own
 // mean and M2 directly; warps merge with shuffles, warps within a CTA through
@@ -41,8 +41,14 @@ namespace cg = cooperative_groups;
 namespace tb {
 namespace {
 
-constexpr int STATS_BLOCK = 256;
-constexpr int STATS_SLOTS = 8;  // cp.async ring slots per thread (16 bytes each)
+#ifndef TB_GN_STATS_BLOCK
+#define TB_GN_STATS_BLOCK 256
+#endif
+#ifndef TB_GN_STATS_SLOTS
+#define TB_GN_STATS_SLOTS 8
+#endif
+constexpr int STATS_BLOCK = TB_GN_STATS_BLOCK;
+constexpr int STATS_SLOTS = TB_GN_STATS_SLOTS;  // cp.async ring slots per thread (16 bytes each)
 constexpr int APPLY_BLOCK = 128;
 constexpr int APPLY_CPT = 4;  // 16-byte chunks per thread per segment
 
@@ -402,6 +408,11 @@ size_t stats_smem(bool aligned) { return aligned ? (size_t)STATS_SLOTS * STATS_B
 template <int DT>
 cudaError_t stats_dt(const GnStatsParams& p, int64_t units, cudaStream_t s) {
     void (*fn)(const GnStatsParams) = stats_fn<DT>(p.aligned != 0);
+    if (stats_smem(p.aligned != 0) > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)stats_smem(p.aligned != 0));
+        if (e != cudaSuccess) return e;
+    }
     if (p.cs > 8) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -438,21 +449,6 @@ cudaError_t apply_dt(const GnApplyParams& p, int64_t items, cudaStream_t s) {
 int gn_apply_segment(int dtype, bool aligned) {
     const int bytes = dtype == F32 ? 4 : 2;
     return APPLY_BLOCK * (aligned ? APPLY_CPT * (16 / bytes) : APPLY_CPT);
-}
-
-int gn_stats_ctas_per_sm(int dtype, bool aligned) {
-    void (*fn)(const GnStatsParams);
-    switch (dtype) {
-        case F32: fn = stats_fn<F32>(aligned); break;
-        case F16: fn = stats_fn<F16>(aligned); break;
-        default: fn = stats_fn<BF16>(aligned); break;
-    }
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, STATS_BLOCK, stats_smem(aligned)) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 1;
-    }
-    return n > 0 ? n : 1;
 }
 
 cudaError_t launch_gn_stats(const GnStatsParams& p, int dtype, int64_t units, cudaStream_t s) {

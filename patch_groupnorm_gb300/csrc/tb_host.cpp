@@ -29,6 +29,13 @@
 #ifndef TB_STITCH_ROWS_PER_THREAD
 #define TB_STITCH_ROWS_PER_THREAD 16
 #endif
+#ifndef TB_STITCH_ROWS_PER_THREAD_3D
+#define TB_STITCH_ROWS_PER_THREAD_3D 64
+#endif
+// Cluster size of the GroupNorm statistics kernel; 0 picks it from occupancy.
+#ifndef TB_GN_FORCE_CS
+#define TB_GN_FORCE_CS 0
+#endif
 
 namespace {
 
@@ -122,19 +129,6 @@ tb_status device_sms(int* sms) {
     return TB_OK;
 }
 
-// statistics-kernel occupancy per (device, dtype, path), cached
-int g_stats_occ[MAX_DEVICES][3][2] = {};
-
-int gn_stats_occupancy(int dtype, bool aligned) {
-    int dev = 0;
-    (void)cudaGetDevice(&dev);
-    if (dev < 0 || dev >= MAX_DEVICES) return tb::gn_stats_ctas_per_sm(dtype, aligned);
-    std::lock_guard<std::mutex> lock(g_mu);
-    int& v = g_stats_occ[dev][dtype][aligned ? 1 : 0];
-    if (v == 0) v = tb::gn_stats_ctas_per_sm(dtype, aligned);
-    return v;
-}
-
 int elem_bytes(tb_dtype d) { return d == TB_F32 ? 4 : 2; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -206,7 +200,7 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     l.dtype = (int)dtype;
     l.vec = vec;
     // Pieces per tile; the grid's second extent is the largest count.
-    const int rpt = TB_STITCH_ROWS_PER_THREAD;
+    const int rpt = ndim == 3 ? TB_STITCH_ROWS_PER_THREAD_3D : TB_STITCH_ROWS_PER_THREAD;
     int max_pieces = 0, max_ebx = 0, max_eby = 0;
     for (int k = 0; k < g[0].n; ++k)
         for (int i = 0; i < g[1].n; ++i)
@@ -226,7 +220,15 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     l.grid_y = max_pieces;
     l.grid_z = 1;
     // vector path: 8 staging slots of 16 bytes per thread, then coefficients
-    l.smem = (vec > 1 ? 8 * tb::STITCH_BLOCK * 16 : 0) + (int)(sizeof(float) * 2 * (size_t)(max_ebx + max_eby));
+    int max_ebt = 0;
+    for (int k = 1; ndim == 3 && k < g[0].n; ++k) max_ebt = std::max(max_ebt, std::min(g[0].blend[k], g[0].kept[k]));
+    l.smem = (vec > 1 ? 8 * tb::STITCH_BLOCK * 16 : 0) +
+             (int)(sizeof(float) * 2 * (size_t)(max_ebx + max_eby + max_ebt));
+    // byte pitches of a frame of any tile and of the output fit 32 bits
+    for (int i = 0; i < g[1].n; ++i)
+        for (int j = 0; j < g[2].n; ++j)
+            if ((int64_t)g[1].ext[i] * g[2].ext[j] * eb > 2147483647LL) return TB_ERR_UNSUPPORTED;
+    if ((int64_t)prm.OH * prm.OW * eb > 2147483647LL) return TB_ERR_UNSUPPORTED;
     if (l.smem > 200 * 1024) return TB_ERR_UNSUPPORTED;
     (void)large;
 
@@ -392,17 +394,18 @@ TB_API tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dty
     prm.P = P;
     prm.G = G;
     prm.aligned = aligned ? 1 : 0;
-    // CTAs per unit (the cluster size, 1..8): as many as keep the whole grid
-    // within one wave of resident CTAs, each streaming >= 16 KB
+    // CTAs per unit (the cluster size, 1..8): about two CTAs per SM in all,
+    // each streaming >= 16 KB.  Measured on GB300: larger clusters of
+    // shorter CTAs lose more to their barriers than they gain in parallelism.
+    const int64_t units = (int64_t)P * N * G;
+    const int64_t bytes = max_len * elem_bytes(dtype);
     int sms = 0;
     s = device_sms(&sms);
     if (s != TB_OK) return s;
-    const int64_t units = (int64_t)P * N * G;
-    const int64_t bytes = max_len * elem_bytes(dtype);
-    const int64_t slots = (int64_t)sms * gn_stats_occupancy((int)dtype, aligned);
-    int64_t cs64 = units > 0 ? slots / units : 1;
+    int64_t cs64 = units > 0 ? (2LL * sms + units / 2) / units : 1;
     cs64 = std::min<int64_t>(cs64, bytes / 16384);
-    const int cs = (int)std::max<int64_t>(1, std::min<int64_t>(8, cs64));
+    int cs = (int)std::max<int64_t>(1, std::min<int64_t>(8, cs64));
+    if (TB_GN_FORCE_CS > 0) cs = TB_GN_FORCE_CS;
     prm.cs = cs;
     if (units * cs > 2147483647LL) return TB_ERR_UNSUPPORTED;
     cudaError_t e = tb::launch_gn_stats(prm, (int)dtype, units, reinterpret_cast<cudaStream_t>(stream));

@@ -89,8 +89,8 @@ __host__ __device__ inline int box_piece_rows(int b, int width, int rows_per_thr
     return bdy * (per > 1 ? per : 1);
 }
 
-// Pieces of one tile: for every non-empty box, one piece per frame and per
-// run of box_piece_rows() rows.  Boxes are enumerated from the most bands to
+// Pieces of one tile: for every non-empty box, one piece per run of
+// box_piece_rows() rows of its (frame, row) space flattened frame-major.  Boxes are enumerated from the most bands to
 // the fewest, so the longest pieces are dispatched first.
 __host__ __device__ inline int tile_pieces(int ndim, int Kt, int Ky, int Kx, int ebt, int eby, int ebx, int vec,
                                            int rows_per_thread) {
@@ -100,7 +100,7 @@ __host__ __device__ inline int tile_pieces(int ndim, int Kt, int Ky, int Kx, int
         const BoxShape s = box_shape(b, Kt, Ky, Kx, ebt, eby, ebx, vec);
         if (s.nt <= 0 || s.ny <= 0 || s.width <= 0) continue;
         const int R = box_piece_rows(b, s.width, rows_per_thread);
-        total += s.nt * ((s.ny + R - 1) / R);
+        total += (s.nt * s.ny + R - 1) / R;  // frames x rows, flattened
     }
     return total;
 }
@@ -166,9 +166,6 @@ int gn_apply_segment(int dtype, bool aligned);
 
 // Records a CUDA error for tb_last_cuda_error() (defined in tb_host.cpp).
 void record_cuda_error(cudaError_t e);
-
-// Resident statistics CTAs per SM (occupancy of the kernel variant).
-int gn_stats_ctas_per_sm(int dtype, bool aligned);
 
 cudaError_t launch_gn_stats(const GnStatsParams& p, int dtype, int64_t units, cudaStream_t s);
 cudaError_t launch_gn_apply(const GnApplyParams& p, int dtype, int64_t items, cudaStream_t s);

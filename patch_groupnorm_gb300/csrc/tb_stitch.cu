@@ -61,7 +61,7 @@
 #define TB_STITCH_MIN_CTAS_2D 4
 #endif
 #ifndef TB_STITCH_MIN_CTAS_3D
-#define TB_STITCH_MIN_CTAS_3D 4
+#define TB_STITCH_MIN_CTAS_3D 3
 #endif
 
 namespace tb {
@@ -234,33 +234,119 @@ __device__ __forceinline__ void eval_nodes(Chunk<DT, VEC> (&F)[NDIM == 3 ? 8 : 4
     }
 }
 
-// Per-CTA description of its box piece.
+// Per-CTA description of its box piece.  A box is `nt` frames x `nyb` rows x
+// `width` chunks of the tile's kept part, starting at frame t0, row y0,
+// column x0 (tile-local); a piece is the rows [rbeg, rend) of the box in
+// frame-major order (row r is frame t0 + r / nyb, row y0 + r % nyb).
 struct Piece {
     int64_t plane;       // (batch, channel) plane
     int k, i, j;         // tile
     int need;            // box bits: 4 time band, 2 height band, 1 width band
-    int ct;              // frame inside the tile (3D)
-    int rbeg, rend;      // rows [rbeg, rend) inside the tile
+    int t0, y0, nyb;     // box origin and rows per frame
+    int rbeg, rend;      // flattened rows of this piece
     int x0, width;       // first column (elements) and width (chunks)
     int bdx, bdy, cpt;   // thread layout
 };
 
-// One box, compiled for its set of source tiles NEED.  Rows are processed UR
-// at a time: all their loads first, then the arithmetic and the stores.
-template <int NDIM, int NEED, int UR, int DT, int VEC, int MAXA, int MAXT, int MAXC>
-__device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p, const Piece& pc,
-                                        const float* s_xw, const float* s_xu, const float* s_yw, const float* s_yu,
-                                        float wt, float ut) {
-    constexpr int NN = NDIM == 3 ? 8 : 4;
-    using C = Chunk<DT, VEC>;
+// Source node m of the box: its tile, and the byte address of the box
+// origin (frame t0, row y0) at column cx.
+template <int NDIM, int DT, int MAXA, int MAXT, int MAXC>
+__device__ __forceinline__ const char* node_origin(const StitchParams<MAXA, MAXT, MAXC>& p, const Piece& pc, int m,
+                                                   int cx) {
     const auto& AT = p.ax[0];
     const auto& AY = p.ax[1];
     const auto& AX = p.ax[2];
+    const int dt = (m >> 2) & 1, dy = (m >> 1) & 1, dx = m & 1;
+    const int kq = pc.k - dt, iq = pc.i - dy, jq = pc.j - dx;
+    const int64_t Lt = NDIM == 3 ? AT.ext[kq] : 1;
+    const int64_t Ly = AY.ext[iq];
+    const int64_t Lx = AX.ext[jq];
+    const int lt = NDIM == 3 ? (dt ? AT.ext[pc.k - 1] - AT.blend[pc.k] + pc.t0 : pc.t0) : 0;
+    const int ly = (dy ? AY.ext[pc.i - 1] - AY.blend[pc.i] : 0) + pc.y0;
+    const int lx = dx ? AX.ext[pc.j - 1] - AX.blend[pc.j] + cx : cx;
+    return reinterpret_cast<const char*>(p.tiles[(kq * AY.n + iq) * AX.n + jq]) +
+           (((pc.plane * Lt + lt) * Ly + ly) * Lx + lx) * Elt<DT>::BYTES;
+}
+
+// Byte pitches of one frame and one row in the source tiles: row pitch by
+// width-neighbour bit dx, frame pitch by (dy, dx).
+struct Pitches {
+    int32_t row[2];
+    int32_t frame[2][2];
+    int32_t orow, oframe;  // output
+};
+
+template <int DT, int MAXA, int MAXT, int MAXC>
+__device__ __forceinline__ Pitches make_pitches(const StitchParams<MAXA, MAXT, MAXC>& p, const Piece& pc) {
+    const auto& AY = p.ax[1];
+    const auto& AX = p.ax[2];
+    Pitches q;
+    for (int dx = 0; dx < 2; ++dx) {
+        const int jq = pc.j - dx >= 0 ? pc.j - dx : 0;
+        q.row[dx] = AX.ext[jq] * Elt<DT>::BYTES;
+        for (int dy = 0; dy < 2; ++dy) {
+            const int iq = pc.i - dy >= 0 ? pc.i - dy : 0;
+            q.frame[dy][dx] = AY.ext[iq] * AX.ext[jq] * Elt<DT>::BYTES;
+        }
+    }
+    q.orow = p.OW * Elt<DT>::BYTES;
+    q.oframe = p.OH * p.OW * Elt<DT>::BYTES;
+    return q;
+}
+
+template <int NDIM, int DT, int MAXA, int MAXT, int MAXC>
+__device__ __forceinline__ char* out_origin(const StitchParams<MAXA, MAXT, MAXC>& p, const Piece& pc, int cx) {
+    const auto& AT = p.ax[0];
+    const auto& AY = p.ax[1];
+    const auto& AX = p.ax[2];
+    const int64_t ot = NDIM == 3 ? AT.off[pc.k] + pc.t0 : 0;
+    return reinterpret_cast<char*>(p.out) +
+           (((pc.plane * p.OT + ot) * p.OH + AY.off[pc.i] + pc.y0) * (int64_t)p.OW + AX.off[pc.j] + cx) *
+               Elt<DT>::BYTES;
+}
+
+// A thread's position in the box: frame and row relative to the box origin
+// (a 2D box has one frame).
+template <int NDIM>
+struct RowPos {
+    int ft, fy;
+    __device__ __forceinline__ void set(int r, int nyb) {
+        if constexpr (NDIM == 3) {
+            ft = r / nyb;
+            fy = r - ft * nyb;
+        } else {
+            ft = 0;
+            fy = r;
+        }
+    }
+    __device__ __forceinline__ void advance(int by, int nyb) {
+        fy += by;
+        if constexpr (NDIM == 3) {
+            while (fy >= nyb) {
+                fy -= nyb;
+                ++ft;
+            }
+        }
+    }
+    // byte offset of this position for frame / row pitches
+    __device__ __forceinline__ int64_t off(int32_t frame_pitch, int32_t row_pitch) const {
+        if constexpr (NDIM == 3) return (int64_t)ft * frame_pitch + (int64_t)fy * row_pitch;
+        return (int64_t)fy * row_pitch;
+    }
+};
+
+// One box, compiled for its set of source tiles NEED (element path).  Rows
+// are processed UR at a time: all their loads first, then the arithmetic.
+template <int NDIM, int NEED, int UR, int DT, int VEC, int MAXA, int MAXT, int MAXC>
+__device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p, const Piece& pc,
+                                        const float* s_xw, const float* s_xu, const float* s_yw, const float* s_yu,
+                                        const float* s_tw, const float* s_tu) {
+    constexpr int NN = NDIM == 3 ? 8 : 4;
+    using C = Chunk<DT, VEC>;
     const int tx = threadIdx.x % pc.bdx;
     const int ty = threadIdx.x / pc.bdx;
     if (ty >= pc.bdy) return;
-    const int ny = AY.n, nx = AX.n;
-    const int64_t plane = pc.plane;
+    const Pitches pt = make_pitches<DT>(p, pc);
     for (int q = 0; q < pc.cpt; ++q) {
         const int c = tx + q * pc.bdx;
         if (c >= pc.width) break;
@@ -273,39 +359,24 @@ __device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p,
                 xu[l] = s_xu[cx + l];
             }
         }
-        // per source node: address of its row-0 chunk and its row pitch in bytes
-        const char* nrow0[NN];
-        int32_t npitch[NN];
+        const char* org[NN];
 #pragma unroll
-        for (int m = 0; m < NN; ++m) {
-            if ((m & ~NEED) != 0) continue;
-            const int dt = (m >> 2) & 1, dy = (m >> 1) & 1, dx = m & 1;
-            const int kq = pc.k - dt, iq = pc.i - dy, jq = pc.j - dx;
-            const int64_t Lt = NDIM == 3 ? AT.ext[kq] : 1;
-            const int64_t Ly = AY.ext[iq];
-            const int64_t Lx = AX.ext[jq];
-            const int lt = NDIM == 3 ? (dt ? AT.ext[pc.k - 1] - AT.blend[pc.k] + pc.ct : pc.ct) : 0;
-            const int ly0 = dy ? AY.ext[pc.i - 1] - AY.blend[pc.i] : 0;
-            const int lx = dx ? AX.ext[pc.j - 1] - AX.blend[pc.j] + cx : cx;
-            nrow0[m] = reinterpret_cast<const char*>(p.tiles[(kq * ny + iq) * nx + jq]) +
-                       (((plane * Lt + lt) * Ly + ly0) * Lx + lx) * Elt<DT>::BYTES;
-            npitch[m] = (int32_t)(Lx * Elt<DT>::BYTES);
-        }
-        const int64_t OW = p.OW;
-        char* orow0 = reinterpret_cast<char*>(p.out) +
-                      (((plane * p.OT + (NDIM == 3 ? AT.off[pc.k] + pc.ct : 0)) * (int64_t)p.OH + AY.off[pc.i]) * OW +
-                       AX.off[pc.j] + cx) * Elt<DT>::BYTES;
-        const int32_t opitch = (int32_t)(OW * Elt<DT>::BYTES);
+        for (int m = 0; m < NN; ++m)
+            if ((m & ~NEED) == 0) org[m] = node_origin<NDIM, DT>(p, pc, m, cx);
+        char* oorg = out_origin<NDIM, DT>(p, pc, cx);
         for (int r = pc.rbeg + ty; r < pc.rend; r += UR * pc.bdy) {
             C F[UR][NN];
+            RowPos<NDIM> pos[UR];
 #pragma unroll
             for (int u = 0; u < UR; ++u) {
                 const int ru = r + u * pc.bdy;
+                pos[u].set(ru, pc.nyb);
                 if (ru < pc.rend) {
 #pragma unroll
                     for (int m = 0; m < NN; ++m) {
                         if ((m & ~NEED) != 0) continue;
-                        F[u][m] = load_chunk<DT, VEC>(nrow0[m] + (int64_t)ru * npitch[m], 0);
+                        const int dy = (m >> 1) & 1, dx = m & 1;
+                        F[u][m] = load_chunk<DT, VEC>(org[m] + pos[u].off(pt.frame[dy][dx], pt.row[dx]), 0);
                     }
                 }
             }
@@ -314,15 +385,19 @@ __device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p,
                 const int ru = r + u * pc.bdy;
                 if (ru < pc.rend) {
                     if constexpr (NEED != 0) {
-                        float wy = 0.f, uy = 0.f;
+                        float wy = 0.f, uy = 0.f, wt = 0.f, ut = 0.f;
                         if constexpr ((NEED & 2) != 0) {
-                            wy = s_yw[ru];
-                            uy = s_yu[ru];
+                            wy = s_yw[pc.y0 + pos[u].fy];
+                            uy = s_yu[pc.y0 + pos[u].fy];
+                        }
+                        if constexpr ((NEED & 4) != 0) {
+                            wt = s_tw[pc.t0 + pos[u].ft];
+                            ut = s_tu[pc.t0 + pos[u].ft];
                         }
                         eval_nodes<NDIM, NEED, DT, VEC>(F[u], wt, ut, wy, uy, [&](int l) { return xw[l]; },
                                                         [&](int l) { return xu[l]; });
                     }
-                    store_chunk<DT, VEC>(orow0 + (int64_t)ru * opitch, 0, F[u][0]);
+                    store_chunk<DT, VEC>(oorg + pos[u].off(pt.oframe, pt.orow), 0, F[u][0]);
                 }
             }
         }
@@ -419,27 +494,22 @@ struct RowCtx {
 template <int NDIM, int NEED, int DT, int VEC, int MAXA, int MAXT, int MAXC>
 __device__ __forceinline__ void run_box_pipe(const StitchParams<MAXA, MAXT, MAXC>& p, const Piece& pc,
                                              const float* s_xw, const float* s_xu, const float* s_yw,
-                                             const float* s_yu, float wt, float ut, uint32_t s_slots) {
+                                             const float* s_yu, const float* s_tw, const float* s_tu,
+                                             uint32_t s_slots) {
     constexpr int NN = NDIM == 3 ? 8 : 4;
     constexpr int NU = nodes_of(NEED);
     constexpr int S = stages_of(NEED);
     using C = Chunk<DT, VEC>;
-    const auto& AT = p.ax[0];
-    const auto& AY = p.ax[1];
-    const auto& AX = p.ax[2];
     const int tx = threadIdx.x % pc.bdx;
     const int ty = threadIdx.x / pc.bdx;
     if (ty >= pc.bdy) return;
-    const int ny = AY.n, nx = AX.n;
     // slot (stage st, node rank n) of this thread: [st][n][thread] x 16 bytes,
     // so a warp's 16-byte accesses to one slot are contiguous
     const uint32_t slot_stride = (uint32_t)STITCH_BLOCK * 16u;
     const uint32_t my_slot0 = s_slots + (uint32_t)threadIdx.x * 16u;
-    const int64_t plane = pc.plane;
+    const Pitches pt = make_pitches<DT>(p, pc);
     RowCtx<VEC> ctx;
     ctx.stride = slot_stride;
-    ctx.wt = wt;
-    ctx.ut = ut;
     for (int q = 0; q < pc.cpt; ++q) {
         const int c = tx + q * pc.bdx;
         if (c >= pc.width) break;
@@ -451,36 +521,27 @@ __device__ __forceinline__ void run_box_pipe(const StitchParams<MAXA, MAXT, MAXC
                 ctx.xu[l] = s_xu[cx + l];
             }
         }
-        const char* nrow0[NU];
-        int32_t npitch[NU];
+        const char* org[NU];
 #pragma unroll
-        for (int m = 0; m < NN; ++m) {
-            if ((m & ~NEED) != 0) continue;
-            const int dt = (m >> 2) & 1, dy = (m >> 1) & 1, dx = m & 1;
-            const int kq = pc.k - dt, iq = pc.i - dy, jq = pc.j - dx;
-            const int64_t Lt = NDIM == 3 ? AT.ext[kq] : 1;
-            const int64_t Ly = AY.ext[iq];
-            const int64_t Lx = AX.ext[jq];
-            const int lt = NDIM == 3 ? (dt ? AT.ext[pc.k - 1] - AT.blend[pc.k] + pc.ct : pc.ct) : 0;
-            const int ly0 = dy ? AY.ext[pc.i - 1] - AY.blend[pc.i] : 0;
-            const int lx = dx ? AX.ext[pc.j - 1] - AX.blend[pc.j] + cx : cx;
-            nrow0[node_rank(NEED, m)] = reinterpret_cast<const char*>(p.tiles[(kq * ny + iq) * nx + jq]) +
-                                        (((plane * Lt + lt) * Ly + ly0) * Lx + lx) * Elt<DT>::BYTES;
-            npitch[node_rank(NEED, m)] = (int32_t)(Lx * Elt<DT>::BYTES);
-        }
-        const int64_t OW = p.OW;
-        char* orow0 = reinterpret_cast<char*>(p.out) +
-                      (((plane * p.OT + (NDIM == 3 ? AT.off[pc.k] + pc.ct : 0)) * (int64_t)p.OH + AY.off[pc.i]) * OW +
-                       AX.off[pc.j] + cx) * Elt<DT>::BYTES;
-        const int32_t opitch = (int32_t)(OW * Elt<DT>::BYTES);
+        for (int m = 0; m < NN; ++m)
+            if ((m & ~NEED) == 0) org[node_rank(NEED, m)] = node_origin<NDIM, DT>(p, pc, m, cx);
+        char* oorg = out_origin<NDIM, DT>(p, pc, cx);
 
         const int r0 = pc.rbeg + ty;
         const int nrows = r0 < pc.rend ? (pc.rend - r0 + pc.bdy - 1) / pc.bdy : 0;
-        auto issue = [&](int m) {  // rows r0 + m * bdy into stage m % S
-            const int row = r0 + m * pc.bdy;
+        RowPos<NDIM> ipos, cpos;  // the row being fetched, the row being computed
+        ipos.set(r0, pc.nyb);
+        cpos = ipos;
+        auto issue = [&](int m) {  // the fetch row into stage m % S
             const uint32_t st = my_slot0 + (uint32_t)((m % S) * NU) * slot_stride;
 #pragma unroll
-            for (int n = 0; n < NU; ++n) cp_async16(st + (uint32_t)n * slot_stride, nrow0[n] + (int64_t)row * npitch[n]);
+            for (int mm = 0; mm < NN; ++mm) {
+                if ((mm & ~NEED) != 0) continue;
+                const int dy = (mm >> 1) & 1, dx = mm & 1;
+                const int n = node_rank(NEED, mm);
+                cp_async16(st + (uint32_t)n * slot_stride, org[n] + ipos.off(pt.frame[dy][dx], pt.row[dx]));
+            }
+            ipos.advance(pc.bdy, pc.nyb);
         };
 #pragma unroll
         for (int m = 0; m < S - 1; ++m) {
@@ -491,31 +552,35 @@ __device__ __forceinline__ void run_box_pipe(const StitchParams<MAXA, MAXT, MAXC
             if (m + S - 1 < nrows) issue(m + S - 1);
             cp_async_commit();
             cp_async_wait<S - 1>();
-            const int row = r0 + m * pc.bdy;
             ctx.base = my_slot0 + (uint32_t)((m % S) * NU) * slot_stride;
             if constexpr ((NEED & 2) != 0) {
-                ctx.wy = s_yw[row];
-                ctx.uy = s_yu[row];
+                ctx.wy = s_yw[pc.y0 + cpos.fy];
+                ctx.uy = s_yu[pc.y0 + cpos.fy];
+            }
+            if constexpr ((NEED & 4) != 0) {
+                ctx.wt = s_tw[pc.t0 + cpos.ft];
+                ctx.ut = s_tu[pc.t0 + cpos.ft];
             }
             C F[NN];
             DagEval<NDIM, NEED, 3, DT, VEC>::run(ctx, F);
-            store_chunk<DT, VEC>(orow0 + (int64_t)row * opitch, 0, F[0]);
+            store_chunk<DT, VEC>(oorg + cpos.off(pt.oframe, pt.orow), 0, F[0]);
+            cpos.advance(pc.bdy, pc.nyb);
         }
         cp_async_wait<0>();
     }
 }
 
 template <int NDIM, int DT, int VEC, int MAXA, int MAXT, int MAXC>
-__global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_3D : TB_STITCH_MIN_CTAS_2D)) stitch_kernel(const __grid_constant__ StitchParams<MAXA, MAXT, MAXC> p) {
+__global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_3D : TB_STITCH_MIN_CTAS_2D))
+    stitch_kernel(const __grid_constant__ StitchParams<MAXA, MAXT, MAXC> p) {
     extern __shared__ __align__(16) unsigned char s_dyn[];
     const auto& AT = p.ax[0];
     const auto& AY = p.ax[1];
     const auto& AX = p.ax[2];
 
-    // which tile, which box, which rows
-    // blockIdx.x runs over (plane, tile) with the tile fastest and
-    // blockIdx.y over the tile's pieces, heaviest first: the GPU dispatches
-    // every tile's longest pieces before any short one.
+    // which tile, which box, which rows.  blockIdx.x runs over (plane, tile)
+    // with the tile fastest and blockIdx.y over the tile's pieces, heaviest
+    // first: the GPU dispatches every tile's longest pieces before any short.
     Piece pc;
     const int ntiles = AX.n * AY.n * (NDIM == 3 ? AT.n : 1);
     const int tile = (int)(blockIdx.x % (unsigned)ntiles);
@@ -536,18 +601,20 @@ __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_
         const BoxShape s = box_shape(b, Kt, Ky, Kx, ebt, eby, ebx, VEC);
         if (s.nt <= 0 || s.ny <= 0 || s.width <= 0) continue;
         const int R = box_piece_rows(b, s.width, p.rows_per_thread);
-        const int nyp = (s.ny + R - 1) / R;
-        if (piece < s.nt * nyp) {
+        const int np = (s.nt * s.ny + R - 1) / R;
+        if (piece < np) {
             pc.need = b;
-            pc.ct = s.t0 + piece / nyp;
-            pc.rbeg = s.y0 + (piece % nyp) * R;
-            pc.rend = min(s.y0 + s.ny, pc.rbeg + R);
+            pc.t0 = s.t0;
+            pc.y0 = s.y0;
+            pc.nyb = s.ny;
+            pc.rbeg = piece * R;
+            pc.rend = min(s.nt * s.ny, pc.rbeg + R);
             pc.x0 = s.x0;
             pc.width = s.width;
             box_layout(s.width, pc.bdx, pc.bdy, pc.cpt);
             break;
         }
-        piece -= s.nt * nyp;
+        piece -= np;
     }
     if (pc.need < 0) return;  // this tile has fewer pieces than the grid row
 
@@ -558,6 +625,8 @@ __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_
     float* s_xu = s_xw + ebx;
     float* s_yw = s_xu + ebx;
     float* s_yu = s_yw + eby;
+    float* s_tw = s_yu + eby;
+    float* s_tu = s_tw + ebt;
     if (pc.need & 1)
         for (int c = threadIdx.x; c < ebx; c += blockDim.x) {
             const float2 v = p.coef[AX.coef[pc.j] + c];
@@ -570,50 +639,52 @@ __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_
             s_yw[c] = v.x;
             s_yu[c] = v.y;
         }
-    float wt = 0.f, ut = 0.f;
-    if (pc.need & 4) {
-        const float2 v = p.coef[AT.coef[pc.k] + pc.ct];
-        wt = v.x;
-        ut = v.y;
-    }
+    if (pc.need & 4)
+        for (int c = threadIdx.x; c < ebt; c += blockDim.x) {
+            const float2 v = p.coef[AT.coef[pc.k] + c];
+            s_tw[c] = v.x;
+            s_tu[c] = v.y;
+        }
     __syncthreads();
 
+#define TB_BOX_ARGS p, pc, s_xw, s_xu, s_yw, s_yu, s_tw, s_tu
     if constexpr (VEC * Elt<DT>::BYTES == 16) {
         const uint32_t s_slots = (uint32_t)__cvta_generic_to_shared(s_stage);
         switch (pc.need) {
-            case 0: run_box_pipe<NDIM, 0, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
-            case 1: run_box_pipe<NDIM, 1, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
-            case 2: run_box_pipe<NDIM, 2, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
-            case 3: run_box_pipe<NDIM, 3, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+            case 0: run_box_pipe<NDIM, 0, DT, VEC>(TB_BOX_ARGS, s_slots); break;
+            case 1: run_box_pipe<NDIM, 1, DT, VEC>(TB_BOX_ARGS, s_slots); break;
+            case 2: run_box_pipe<NDIM, 2, DT, VEC>(TB_BOX_ARGS, s_slots); break;
+            case 3: run_box_pipe<NDIM, 3, DT, VEC>(TB_BOX_ARGS, s_slots); break;
             default:
                 if constexpr (NDIM == 3) {
                     switch (pc.need) {
-                        case 4: run_box_pipe<NDIM, 4, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
-                        case 5: run_box_pipe<NDIM, 5, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
-                        case 6: run_box_pipe<NDIM, 6, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
-                        case 7: run_box_pipe<NDIM, 7, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut, s_slots); break;
+                        case 4: run_box_pipe<NDIM, 4, DT, VEC>(TB_BOX_ARGS, s_slots); break;
+                        case 5: run_box_pipe<NDIM, 5, DT, VEC>(TB_BOX_ARGS, s_slots); break;
+                        case 6: run_box_pipe<NDIM, 6, DT, VEC>(TB_BOX_ARGS, s_slots); break;
+                        case 7: run_box_pipe<NDIM, 7, DT, VEC>(TB_BOX_ARGS, s_slots); break;
                     }
                 }
                 break;
         }
     } else {
         switch (pc.need) {
-            case 0: run_box<NDIM, 0, TB_STITCH_UR_COPY, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-            case 1: run_box<NDIM, 1, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-            case 2: run_box<NDIM, 2, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-            case 3: run_box<NDIM, 3, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+            case 0: run_box<NDIM, 0, TB_STITCH_UR_COPY, DT, VEC>(TB_BOX_ARGS); break;
+            case 1: run_box<NDIM, 1, TB_STITCH_UR_ONE, DT, VEC>(TB_BOX_ARGS); break;
+            case 2: run_box<NDIM, 2, TB_STITCH_UR_ONE, DT, VEC>(TB_BOX_ARGS); break;
+            case 3: run_box<NDIM, 3, TB_STITCH_UR_TWO, DT, VEC>(TB_BOX_ARGS); break;
             default:
                 if constexpr (NDIM == 3) {
                     switch (pc.need) {
-                        case 4: run_box<NDIM, 4, TB_STITCH_UR_ONE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-                        case 5: run_box<NDIM, 5, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-                        case 6: run_box<NDIM, 6, TB_STITCH_UR_TWO, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
-                        case 7: run_box<NDIM, 7, TB_STITCH_UR_THREE, DT, VEC>(p, pc, s_xw, s_xu, s_yw, s_yu, wt, ut); break;
+                        case 4: run_box<NDIM, 4, TB_STITCH_UR_ONE, DT, VEC>(TB_BOX_ARGS); break;
+                        case 5: run_box<NDIM, 5, TB_STITCH_UR_TWO, DT, VEC>(TB_BOX_ARGS); break;
+                        case 6: run_box<NDIM, 6, TB_STITCH_UR_TWO, DT, VEC>(TB_BOX_ARGS); break;
+                        case 7: run_box<NDIM, 7, TB_STITCH_UR_THREE, DT, VEC>(TB_BOX_ARGS); break;
                     }
                 }
                 break;
         }
     }
+#undef TB_BOX_ARGS
 }
 
 template <int MAXA, int MAXT, int MAXC>
