@@ -94,16 +94,23 @@ def source_digest(path):
 
 
 def profiled_traffic(kernel_key, src_path):
-    """DRAM bytes per launch recorded by the last ncu capture of this kernel,
-    if that capture was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch (read + write) recorded by the last ncu capture of
+    this kernel on this workload (profiles/traffic.txt), if that capture was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
-        d = json.load(open(p))[kernel_key]
-    except Exception:
-        return None, None
-    if d.get("source_sha256_16") != source_digest(src_path):
-        return None, d.get("capture")
-    return d.get("dram_bytes_per_launch"), d.get("capture")
+        for line in open(p):
+            if line.startswith("#") or not line.strip():
+                continue
+            f = line.split()
+            if f[0] != kernel_key:
+                continue
+            if f[5] != source_digest(os.path.join(ROOT, f[4])):
+                return None, f[6] + " (kernel source changed since)"
+            return int(f[1]), f[6]
+    except OSError:
+        pass
+    return None, None
 
 
 class ClockSampler:
@@ -303,8 +310,7 @@ def run_ours(args):
         # keep the pinned buffers alive until here
         del host_tiles, host_out
 
-    traffic, capture = profiled_traffic("stitch2d/" + args.workload,
-                                        os.path.join(ROOT, "patch_groupnorm_gb300", "csrc", "tb_stitch.cu"))
+    traffic, capture = profiled_traffic("stitch2d/" + args.workload, None)
     roofline = {"kernel": "tb::stitch_kernel<2D,bf16>", "bound": "hbm", "achieved": round(gbs, 1),
                 "peak": peak, "peak_kind": "%s (%s)" % (peak_kind, "burst copy, kernel timed alone"),
                 "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": traffic,
