@@ -57,6 +57,12 @@
 #ifndef TB_STITCH_UR_THREE
 #define TB_STITCH_UR_THREE 1
 #endif
+// Programmatic dependent launch: the kernel's parameter-only prologue may
+// overlap the previous kernel in the stream; it waits for that kernel before
+// its first global-memory access.
+#ifndef TB_STITCH_PDL
+#define TB_STITCH_PDL 1
+#endif
 #ifndef TB_STITCH_MIN_CTAS_2D
 #define TB_STITCH_MIN_CTAS_2D 4
 #endif
@@ -646,6 +652,11 @@ __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_
             s_tu[c] = v.y;
         }
     __syncthreads();
+#if TB_STITCH_PDL
+    // everything above read kernel parameters only; from here on the tiles
+    // and the output are touched, so the preceding grid must be complete
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
 
 #define TB_BOX_ARGS p, pc, s_xw, s_xu, s_yw, s_yu, s_tw, s_tu
     if constexpr (VEC * Elt<DT>::BYTES == 16) {
@@ -719,8 +730,17 @@ cudaError_t launch(const StitchParams<MAXA, MAXT, MAXC>& p, const StitchLaunch& 
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem);
         if (e != cudaSuccess) return e;
     }
-    fn<<<dim3(l.grid_x, l.grid_y, l.grid_z), STITCH_BLOCK, l.smem, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(l.grid_x, l.grid_y, l.grid_z);
+    cfg.blockDim = dim3(STITCH_BLOCK, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)l.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = TB_STITCH_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 }  // namespace

@@ -10,6 +10,7 @@ There is no fallback: if the compiled library is missing, importing this
 module raises.
 """
 import ctypes
+import functools
 import os
 from dataclasses import dataclass
 from typing import List, Optional, Sequence, Tuple
@@ -128,8 +129,10 @@ class Layout:
     out_extent: int
 
 
+@functools.lru_cache(maxsize=256)
 def tb_axis_layout(axis: Axis) -> Layout:
-    """The library's derived geometry of one axis (host only)."""
+    """The library's derived geometry of one axis (host only; cached per
+    parameter set)."""
     a = axis.c()
     n = ctypes.c_int32(0)
     cap = TB_MAX_TILES_PER_AXIS
@@ -183,14 +186,16 @@ def tb_stitch2d(tiles: Sequence[Sequence[torch.Tensor]], ay: Axis, ax: Axis, out
     ptrs = []
     if len(tiles) != ly.n:
         raise ValueError("expected %d tile rows, got %d" % (ly.n, len(tiles)))
+    dt = out.dtype
     for i, row in enumerate(tiles):
         if len(row) != lx.n:
             raise ValueError("expected %d tiles in row %d, got %d" % (lx.n, i, len(row)))
+        Ly = ly.extents[i]
         for j, t in enumerate(row):
-            _cuda_contig(t, "tile (%d,%d)" % (i, j))
-            if t.dtype != out.dtype or tuple(t.shape) != (B, C, ly.extents[i], lx.extents[j]):
+            if t.dtype != dt or t.shape != (B, C, Ly, lx.extents[j]) or not t.is_cuda or not t.is_contiguous():
+                _cuda_contig(t, "tile (%d,%d)" % (i, j))
                 raise ValueError("tile (%d,%d) has %s %s, expected %s %s" % (
-                    i, j, t.dtype, tuple(t.shape), out.dtype, (B, C, ly.extents[i], lx.extents[j])))
+                    i, j, t.dtype, tuple(t.shape), dt, (B, C, Ly, lx.extents[j])))
             ptrs.append(t.data_ptr())
     a_y, a_x = ay.c(), ax.c()
     _check(_lib.tb_stitch2d(_ptr_array(ptrs), _dtype_code(out), B, C, ctypes.byref(a_y), ctypes.byref(a_x),
