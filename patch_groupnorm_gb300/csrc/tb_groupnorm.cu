@@ -26,6 +26,10 @@
 // shared memory, and the CTAs of the cluster through distributed shared
 // memory, in a fixed order (deterministic results).
 //
+// Both kernels are launched with programmatic stream serialisation: their
+// parameter-only prologue may overlap the preceding kernel, and they execute
+// griddepcontrol.wait before touching global memory.
+//
 // gn_apply_kernel: one CTA per segment of one channel row.  Every warp
 // combines the P partials of its group (lane q holds patch q), forms
 // a = rstd * gamma[c] and b = beta[c] - mean * a, and the elements become
@@ -205,6 +209,9 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
     const int64_t start = ((int64_t)n * p.C + (int64_t)g * cg_) * S;
     const char* base = reinterpret_cast<const char*>(p.patches[pp]) + start * GElt<DT>::BYTES;
 
+    // parameters only above; the patches may be written by the preceding grid
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     Stat acc{0.f, 0.f, 0.f};
     if constexpr (VECTOR) {
         // len and start are multiples of VEC: whole 16-byte chunks.  Each
@@ -341,6 +348,8 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
     const int64_t e_begin = seg * p.seg;
     const int64_t e_end = min(S, e_begin + p.seg);
     const int64_t row_start = (int64_t)row * S;
+    // parameters only above; patches and partials come from preceding grids
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if constexpr (VECTOR) {
         // S and every row start are multiples of VEC; issue the data loads first
@@ -422,13 +431,15 @@ cudaError_t stats_dt(const GnStatsParams& p, int64_t units, cudaStream_t s) {
     cfg.blockDim = dim3(STATS_BLOCK, 1, 1);
     cfg.dynamicSmemBytes = stats_smem(p.aligned != 0);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)p.cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
@@ -440,8 +451,17 @@ cudaError_t apply_dt(const GnApplyParams& p, int64_t items, cudaStream_t s) {
     } else {
         fn = p.silu ? gn_apply_kernel<DT, false, 1> : gn_apply_kernel<DT, false, 0>;
     }
-    fn<<<(unsigned)items, APPLY_BLOCK, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)items, 1, 1);
+    cfg.blockDim = dim3(APPLY_BLOCK, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 }  // namespace
