@@ -89,6 +89,24 @@ def stitch_bytes(layouts, planes, esize):
     return planes * (tile_elems + out_elems) * esize, planes * tile_elems * esize, planes * out_elems * esize
 
 
+def ramp_bytes(ay, ax, planes, esize):
+    """Algorithmic bytes of a normalised-ramp stitch: every tile sample with
+    positive weight read once, plus the output written once."""
+    def positive(a):
+        n = len(a.origins)
+        counts = []
+        for t in range(n):
+            c = 0
+            for q in range(a.tile_extent):
+                lo = t == 0 or q - a.zero > 0
+                hi = t == n - 1 or (a.tile_extent - 1 - q) - a.zero > 0
+                c += 1 if (lo and hi) else 0
+            counts.append(c)
+        return counts
+    py, px = positive(ay), positive(ax)
+    return planes * (sum(y * x for y in py for x in px) + ay.out_extent * ax.out_extent) * esize
+
+
 def source_digest(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
@@ -432,6 +450,20 @@ def per_kernel(torch, tb, W, dev, peak, reps):
                     for _ in range(ns)]
             timed(lambda q: tb.tb_stitch3d(sets[q][0], axes[0], axes[1], axes[2], sets[q][1]), ns, nbytes,
                   "stitch3d", name)
+        del sets
+        torch.cuda.empty_cache()
+    for name, w in W.RAMP.items():
+        ay = tb.RampAxis.spread(w.latent_hw[0], w.latent_tile, w.n_tiles[0], w.scale)
+        ax = tb.RampAxis.spread(w.latent_hw[1], w.latent_tile, w.n_tiles[1], w.scale)
+        tiles = W.make_ramp_tiles(w, ay, ax)
+        esize = 4 if w.dtype == "f32" else 2
+        nbytes = ramp_bytes(ay, ax, w.B * w.C, esize)
+        tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+        ns = nsets_for(nbytes)
+        shape = (w.B, w.C, ay.out_extent, ax.out_extent)
+        sets = [([[t.to(dev) for t in row] for row in tiles], torch.empty(shape, dtype=tdt, device=dev))
+                for _ in range(ns)]
+        timed(lambda q: tb.tb_stitch2d_ramp(sets[q][0], ay, ax, sets[q][1]), ns, nbytes, "stitch2d_ramp", name)
         del sets
         torch.cuda.empty_cache()
     for name, w in W.GROUPNORM.items():

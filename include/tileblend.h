@@ -177,6 +177,56 @@ tb_status tb_stitch3d(const void* const* tiles, tb_dtype dtype, int64_t B, int64
                       int64_t out_w, void* stream);
 
 /*
+ * One axis of a normalised-ramp tile layout [STU]: n_tiles tiles of one
+ * extent, placed by the caller (a planner spreads them so the first starts at
+ * 0 and the last ends at out_extent).
+ *   n_tiles      1 .. TB_MAX_TILES_PER_AXIS
+ *   tile_extent  samples per tile (>= 1)
+ *   out_extent   samples of the canvas
+ *   zero         samples of zero weight next to an edge shared with another
+ *                tile (4 latents * scale on the page)
+ *   ramp         samples over which the weight then rises to 1 (8 latents *
+ *                scale on the page; >= 1)
+ *   origins      host array of n_tiles origins in samples, strictly
+ *                ascending, origins[0] == 0, origins[n-1] + tile_extent ==
+ *                out_extent
+ * A tile's weight at distance d (samples) from a shared edge is
+ * clamp((d - zero) / ramp, 0, 1); edges of the canvas carry no ramp.
+ */
+typedef struct {
+    int32_t n_tiles;
+    int32_t tile_extent;
+    int32_t out_extent;
+    int32_t zero;
+    int32_t ramp;
+    const int64_t* origins;
+} tb_ramp_axis;
+
+/* Most tiles with positive weight at one position of a ramp axis. */
+#define TB_RAMP_MAX_COVER 4
+
+/*
+ * tb_stitch2d_ramp -- stitch a 2D grid of equally sized overlapping tiles by
+ * the normalised-ramp blend [STU]: every output sample is the average of the
+ * tiles covering it, weighted by the product of each tile's ramps along both
+ * axes, out = sum(w * x) / sum(w), computed in fp32 and rounded once into the
+ * storage type.  Used for decoded tiles (scale = the VAE's) and for latent
+ * tiles of a tiled encode (scale 1).
+ *
+ *   tiles     host array of ay->n_tiles * ax->n_tiles device pointers,
+ *             row-major; every tile is [B, C, ay->tile_extent, ax->tile_extent]
+ *   out       device [B, C, ay->out_extent, ax->out_extent]; must not
+ *             overlap a tile
+ * Errors: TB_ERR_NULL, TB_ERR_DTYPE, TB_ERR_SHAPE (negative sizes),
+ * TB_ERR_GEOMETRY (origins out of order, not covering the canvas, or a
+ * sample with no positive weight), TB_ERR_UNSUPPORTED (more than
+ * TB_RAMP_MAX_COVER tiles with positive weight at one position, more than
+ * TB_MAX_TILES tiles), TB_ERR_CUDA.
+ */
+tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C, const tb_ramp_axis* ay,
+                           const tb_ramp_axis* ax, void* out, void* stream);
+
+/*
  * tb_patch_gn_stats -- per-patch GroupNorm partial statistics [DVA].
  * An activation [N, C, *spatial] is split along one spatial axis into P
  * patches (the ranks' shards in the pages' patch-parallel decode); patch p is

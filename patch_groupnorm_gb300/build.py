@@ -26,6 +26,7 @@ UNITS = {
     "tb_stitch.cu": ["-fmad=false"],
     "tb_groupnorm.cu": [],
     "tb_noalloc.cu": [],
+    "tb_ramp.cu": [],
 }
 HEADERS = ["tb_internal.h"]
 

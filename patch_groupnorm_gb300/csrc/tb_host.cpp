@@ -315,6 +315,75 @@ tb_status gn_validate(const void* const* patches, int32_t P, tb_dtype dtype, int
 
 void tb::record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
+// ---------------------------------------------------------------------------
+// normalised-ramp stitch
+// ---------------------------------------------------------------------------
+
+// Weight of tile n (of N, extent T) at tile-local position q.
+double ramp_w(int n, int N, int T, int q, int zero, int ramp) {
+    double w = 1.0;
+    if (n > 0) w *= std::min(1.0, std::max(0.0, (double)(q - zero) / ramp));
+    if (n < N - 1) w *= std::min(1.0, std::max(0.0, (double)((T - 1 - q) - zero) / ramp));
+    return w;
+}
+
+// Validates one axis and cuts it into segments of constant positive-weight
+// tile sets, positions grouped `gran` at a time.
+tb_status ramp_axis(const tb_ramp_axis* a, int gran, tb::RampAxisK& k) {
+    if (a == nullptr || a->origins == nullptr) return TB_ERR_NULL;
+    const int N = a->n_tiles, T = a->tile_extent, out = a->out_extent;
+    if (N < 1 || T < 1 || out < 1 || a->zero < 0 || a->ramp < 1) return TB_ERR_GEOMETRY;
+    if (N > tb::RAMP_MAXA) return TB_ERR_UNSUPPORTED;
+    if (a->origins[0] != 0 || a->origins[N - 1] + T != out) return TB_ERR_GEOMETRY;
+    for (int n = 1; n < N; ++n)
+        if (a->origins[n] <= a->origins[n - 1] || a->origins[n] > out - T) return TB_ERR_GEOMETRY;
+    k.n = N;
+    k.T = T;
+    k.out = out;
+    k.zero = a->zero;
+    k.inv_ramp = (float)(1.0 / a->ramp);
+    for (int n = 0; n < N; ++n) k.org[n] = (int32_t)a->origins[n];
+    k.nseg = 0;
+    int cur[tb::RAMP_MAXCOVER] = {-1, -1, -1}, ncur = -1;
+    for (int p0 = 0; p0 < out; p0 += gran) {
+        // tiles with positive weight at any of positions p0 .. p0 + gran - 1
+        int set[tb::RAMP_MAXCOVER], ns = 0;
+        for (int n = 0; n < N; ++n) {
+            bool pos = false;
+            for (int p = p0; p < p0 + gran && p < out; ++p) {
+                const int q = p - (int)a->origins[n];
+                if (q >= 0 && q < T && ramp_w(n, N, T, q, a->zero, a->ramp) > 0.0) pos = true;
+            }
+            if (!pos) continue;
+            if (ns == tb::RAMP_MAXCOVER) return TB_ERR_UNSUPPORTED;
+            set[ns++] = n;
+        }
+        // every single position must have some positive weight
+        for (int p = p0; p < p0 + gran && p < out; ++p) {
+            double sum = 0.0;
+            for (int e = 0; e < ns; ++e) {
+                const int q = p - (int)a->origins[set[e]];
+                if (q >= 0 && q < T) sum += ramp_w(set[e], N, T, q, a->zero, a->ramp);
+            }
+            if (!(sum > 0.0)) return TB_ERR_GEOMETRY;
+        }
+        bool same = ns == ncur;
+        for (int e = 0; same && e < ns; ++e) same = set[e] == cur[e];
+        if (!same) {
+            if (k.nseg == tb::RAMP_MAXSEG) return TB_ERR_UNSUPPORTED;
+            k.seg_start[k.nseg] = p0;
+            k.seg_len[k.nseg] = 0;
+            k.seg_n[k.nseg] = ns;
+            for (int e = 0; e < tb::RAMP_MAXCOVER; ++e) k.seg_tile[k.nseg][e] = (int8_t)(e < ns ? set[e] : 0);
+            ++k.nseg;
+            ncur = ns;
+            for (int e = 0; e < ns; ++e) cur[e] = set[e];
+        }
+        k.seg_len[k.nseg - 1] += std::min(gran, out - p0);
+    }
+    return TB_OK;
+}
+
 // ===========================================================================
 // C ABI
 // ===========================================================================
@@ -368,6 +437,64 @@ TB_API tb_status tb_stitch3d(const void* const* tiles, tb_dtype dtype, int64_t B
                              int64_t out_w, void* stream) {
     if (at == nullptr) return TB_ERR_NULL;
     return stitch_common(3, tiles, dtype, B, C, at, ay, ax, out, out_t, out_h, out_w, stream);
+}
+
+TB_API tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
+                                  const tb_ramp_axis* ay, const tb_ramp_axis* ax, void* out, void* stream) {
+    if (dtype != TB_F32 && dtype != TB_F16 && dtype != TB_BF16) return TB_ERR_DTYPE;
+    if (B < 0 || C < 0) return TB_ERR_SHAPE;
+    if (ay == nullptr || ax == nullptr) return TB_ERR_NULL;
+    const int eb = elem_bytes(dtype);
+    const int64_t planes = B * C;
+    if (B > 0 && planes / B != C) return TB_ERR_SHAPE;
+    // 16-byte chunks along the width when the layout and every pointer allow
+    int vec = 16 / eb;
+    bool ok = ax->tile_extent % vec == 0 && ax->out_extent % vec == 0 && ax->origins != nullptr;
+    for (int n = 0; ok && n < ax->n_tiles && n < tb::RAMP_MAXA; ++n) ok = ax->origins[n] % vec == 0;
+    tb::RampParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    tb_status st = ramp_axis(ay, 1, prm.ay);
+    if (st != TB_OK) return st;
+    st = ramp_axis(ax, 1, prm.ax);  // validates the width axis element by element
+    if (st != TB_OK) return st;
+    const int64_t ntiles = (int64_t)ay->n_tiles * ax->n_tiles;
+    if (ntiles > TB_MAX_TILES) return TB_ERR_UNSUPPORTED;
+    if (planes == 0) return TB_OK;
+    if (tiles == nullptr || out == nullptr) return TB_ERR_NULL;
+    for (int64_t q = 0; q < ntiles; ++q)
+        if (tiles[q] == nullptr) return TB_ERR_NULL;
+    if ((int64_t)ay->tile_extent * ax->tile_extent * eb > 2147483647LL ||
+        (int64_t)ax->out_extent * eb > 2147483647LL)
+        return TB_ERR_UNSUPPORTED;
+    ok = ok && aligned16(out);
+    for (int64_t q = 0; ok && q < ntiles; ++q) ok = aligned16(tiles[q]);
+    if (ok) {
+        st = ramp_axis(ax, vec, prm.ax);  // chunk-granular width segments
+        if (st == TB_ERR_UNSUPPORTED) ok = false;
+        else if (st != TB_OK) return st;
+    }
+    if (!ok) {
+        vec = 1;
+        st = ramp_axis(ax, 1, prm.ax);
+        if (st != TB_OK) return st;
+    }
+    for (int64_t q = 0; q < ntiles; ++q) prm.tiles[q] = tiles[q];
+    prm.out = out;
+    prm.planes = planes;
+    int max_pieces = 1;
+    for (int sx = 0; sx < prm.ax.nseg; ++sx) {
+        const int width = prm.ax.seg_len[sx] / vec;
+        const int bdx = std::max(1, std::min(width, tb::ramp_block()));
+        const int bdy = tb::ramp_block() / bdx;
+        prm.rows_per_piece[sx] = bdy * 16;
+        for (int sy = 0; sy < prm.ay.nseg; ++sy)
+            max_pieces = std::max(max_pieces, (prm.ay.seg_len[sy] + prm.rows_per_piece[sx] - 1) / prm.rows_per_piece[sx]);
+    }
+    const int64_t gx = planes * prm.ay.nseg * prm.ax.nseg;
+    if (gx > 2147483647LL || max_pieces > 65535) return TB_ERR_UNSUPPORTED;
+    cudaError_t e = tb::launch_ramp(prm, (int)dtype, vec, (int)gx, max_pieces, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return TB_OK;
 }
 
 TB_API tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dtype dtype, int64_t N, int64_t C,

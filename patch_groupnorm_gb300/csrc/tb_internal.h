@@ -121,6 +121,40 @@ cudaError_t launch_stitch_small(const StitchParamsSmall& p, const StitchLaunch& 
 cudaError_t launch_stitch_large(const StitchParamsLarge& p, const StitchLaunch& l, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
+// Normalised-ramp stitch
+// ---------------------------------------------------------------------------
+
+constexpr int RAMP_MAXA = 64;              // tiles per axis
+constexpr int RAMP_MAXSEG = 2 * RAMP_MAXA + 1;
+constexpr int RAMP_MAXCOVER = 3;           // tiles with positive weight at one position
+
+// One axis as the ramp kernel sees it: the tiles, and the axis cut into
+// segments over which the set of tiles with positive weight is constant.
+struct RampAxisK {
+    int32_t n, T, out, zero;
+    float inv_ramp;
+    int32_t org[RAMP_MAXA];
+    int32_t nseg;
+    int32_t seg_start[RAMP_MAXSEG];
+    int32_t seg_len[RAMP_MAXSEG];
+    int32_t seg_n[RAMP_MAXSEG];
+    int8_t seg_tile[RAMP_MAXSEG][RAMP_MAXCOVER];
+};
+
+struct RampParams {
+    const void* tiles[1024];
+    void* out;
+    int64_t planes;
+    RampAxisK ay, ax;
+    int32_t rows_per_piece[RAMP_MAXSEG];  // by width segment
+};
+static_assert(sizeof(RampParams) <= 32000, "kernel parameter block too large");
+
+int ramp_block();
+int ramp_smem();
+cudaError_t launch_ramp(const RampParams& p, int dtype, int vec, int grid_x, int grid_y, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // PatchGroupNorm
 // ---------------------------------------------------------------------------
 

@@ -1,0 +1,326 @@
+// tb_ramp.cu -- normalised-ramp tile stitch for sm_103a.
+//
+// What is computed (page "Studio: size seam-free VAE tiles from measured
+// peaks", unsloth PR #12764, commit "Decode this VAE in 32-latent tiles ..."):
+// equally sized tiles overlap; a tile has no weight within `zero` samples of
+// an edge it shares with another tile and its weight then rises linearly to
+// 1 over `ramp` samples; the weights are normalised to 1 at every sample.
+// Output = sum over covering tiles of w_y * w_x * x, divided by the sum of
+// the weights -- computed in fp32 and rounded once into the storage type.
+//
+// How.  The weight of a tile factorises over the axes and so does the
+// normaliser, so the normalised weight of tile (a, b) is wy_a * wx_b with
+// wy, wx normalised per axis.  The host cuts each axis into segments over
+// which the set of tiles with positive weight is constant (at 16-byte chunk
+// granularity along the width); the canvas then splits into rectangles with
+// a fixed number of source tiles.  A CTA takes a run of rows of one
+// rectangle for one (batch, channel) plane and runs a path compiled for its
+// (height cover, width cover) in {1, 2, 3}^2; a rectangle covered by one tile
+// is an exact copy (w / w = 1).  Loads stream through a per-thread cp.async
+// ring in shared memory, as in the recurrence stitch.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tb_internal.h"
+
+namespace tb {
+namespace {
+
+template <int DT>
+struct RElt;
+template <>
+struct RElt<F32> {
+    static constexpr int BYTES = 4;
+    __device__ __forceinline__ static void unpack2(uint32_t v, float& lo, float&) { lo = __uint_as_float(v); }
+};
+template <>
+struct RElt<F16> {
+    static constexpr int BYTES = 2;
+    __device__ __forceinline__ static void unpack2(uint32_t v, float& lo, float& hi) {
+        float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+        lo = f.x;
+        hi = f.y;
+    }
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+};
+template <>
+struct RElt<BF16> {
+    static constexpr int BYTES = 2;
+    __device__ __forceinline__ static void unpack2(uint32_t v, float& lo, float& hi) {
+        lo = __uint_as_float(v << 16);
+        hi = __uint_as_float(v & 0xffff0000u);
+    }
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gptr) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds16(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    return v;
+}
+
+// Weight of a tile of extent T at tile-local position q, with ramps on the
+// shared edges (lo: an edge at the start, hi: an edge at the end).
+__device__ __forceinline__ float ramp_weight(int q, int T, bool lo, bool hi, int zero, float inv_ramp) {
+    float w = 1.f;
+    if (lo) w *= fminf(1.f, fmaxf(0.f, (float)(q - zero) * inv_ramp));
+    if (hi) w *= fminf(1.f, fmaxf(0.f, (float)((T - 1 - q) - zero) * inv_ramp));
+    return w;
+}
+
+// 16-byte chunk -> floats
+template <int DT, int VEC>
+__device__ __forceinline__ void unpack_chunk(const uint4& v, float (&x)[VEC]) {
+    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (RElt<DT>::BYTES == 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[q] = __uint_as_float(wd[q]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) RElt<DT>::unpack2(wd[q], x[2 * q], x[2 * q + 1]);
+    }
+}
+// floats -> storage, rounded once (element path: the value sits in .x)
+template <int DT, int VEC>
+__device__ __forceinline__ uint4 acc_pack(const float (&a)[VEC]) {
+    if constexpr (VEC == 1) {
+        if constexpr (RElt<DT>::BYTES == 4) return make_uint4(__float_as_uint(a[0]), 0, 0, 0);
+        else return make_uint4(RElt<DT>::pack2(a[0], 0.f) & 0xffffu, 0, 0, 0);
+    } else if constexpr (RElt<DT>::BYTES == 4) {
+        return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]), __float_as_uint(a[3]));
+    } else {
+        return make_uint4(RElt<DT>::pack2(a[0], a[1]), RElt<DT>::pack2(a[2], a[3]), RElt<DT>::pack2(a[4], a[5]),
+                          RElt<DT>::pack2(a[6], a[7]));
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t load_elem(const char* p) {
+    if constexpr (RElt<DT>::BYTES == 4) return __ldcs(reinterpret_cast<const unsigned int*>(p));
+    else return __ldcs(reinterpret_cast<const unsigned short*>(p));
+}
+template <int DT>
+__device__ __forceinline__ float elem_value(uint32_t v) {
+    float lo, hi = 0.f;
+    RElt<DT>::unpack2(v, lo, hi);
+    return lo;
+}
+template <int DT>
+__device__ __forceinline__ void store_elem(char* p, uint32_t v) {
+    if constexpr (RElt<DT>::BYTES == 4) __stcs(reinterpret_cast<unsigned int*>(p), v);
+    else __stcs(reinterpret_cast<unsigned short*>(p), (unsigned short)(v & 0xffffu));
+}
+
+constexpr int RAMP_BLOCK = 256;
+constexpr int RAMP_SLOTS = 9;  // per thread, 16 bytes each
+
+template <int NA>
+__device__ __forceinline__ float axis_w(const RampAxisK& A, int seg, int a, int pos) {
+    const int t = A.seg_tile[seg][a];
+    return ramp_weight(pos - A.org[t], A.T, t > 0, t < A.n - 1, A.zero, A.inv_ramp);
+}
+
+template <int CY, int CX, int DT, int VEC>
+__device__ __forceinline__ void run_rect(const RampParams& p, int64_t plane, int sy, int sx, int rbeg, int rend,
+                                         uint32_t s_ring) {
+    constexpr int NU = CY * CX;
+    constexpr int S = RAMP_SLOTS / NU >= 2 ? RAMP_SLOTS / NU : 1;
+    const RampAxisK& AY = p.ay;
+    const RampAxisK& AX = p.ax;
+    const int width = AX.seg_len[sx] / VEC;  // chunks
+    const int bdx = width < RAMP_BLOCK ? width : RAMP_BLOCK;
+    const int bdy = RAMP_BLOCK / bdx;
+    const int tx = threadIdx.x % bdx;
+    const int ty = threadIdx.x / bdx;
+    if (ty >= bdy) return;
+    const uint32_t slot_stride = RAMP_BLOCK * 16u;
+    const uint32_t my_slot = s_ring + threadIdx.x * 16u;
+    for (int c = tx; c < width; c += bdx) {
+        const int x0 = AX.seg_start[sx] + c * VEC;
+        // normalised width weights of this chunk's lanes
+        float wx[CX][VEC];
+        if constexpr (CX > 1) {
+#pragma unroll
+            for (int l = 0; l < VEC; ++l) {
+                float sum = 0.f;
+#pragma unroll
+                for (int b = 0; b < CX; ++b) {
+                    wx[b][l] = axis_w<CX>(AX, sx, b, x0 + l);
+                    sum += wx[b][l];
+                }
+                const float inv = 1.0f / sum;
+#pragma unroll
+                for (int b = 0; b < CX; ++b) wx[b][l] *= inv;
+            }
+        }
+        // sources: tile (Y.tile[a], X.tile[b]) at row 0 of the canvas
+        const char* src[NU];
+        int32_t pitch[CX];
+#pragma unroll
+        for (int b = 0; b < CX; ++b) pitch[b] = AX.T * RElt<DT>::BYTES;
+#pragma unroll
+        for (int a = 0; a < CY; ++a)
+#pragma unroll
+            for (int b = 0; b < CX; ++b) {
+                const int ti = AY.seg_tile[sy][a], tj = AX.seg_tile[sx][b];
+                // element (plane, y - oy, x0 - ox) of tile (ti, tj) is src + y * pitch
+                src[a * CX + b] = reinterpret_cast<const char*>(p.tiles[ti * AX.n + tj]) +
+                                  (((plane * AY.T) - AY.org[ti]) * (int64_t)AX.T + (x0 - AX.org[tj])) *
+                                      RElt<DT>::BYTES;
+            }
+        char* dst = reinterpret_cast<char*>(p.out) + ((plane * AY.out) * (int64_t)AX.out + x0) * RElt<DT>::BYTES;
+        const int32_t opitch = AX.out * RElt<DT>::BYTES;
+
+        const int r0 = rbeg + ty;
+        const int nrows = r0 < rend ? (rend - r0 + bdy - 1) / bdy : 0;
+        // combine the CY x CX source values of one row; x_ab(l) reads them
+        auto combine = [&](int y, auto x_ab) {
+            float wy[CY];
+            if constexpr (CY > 1) {
+                float sum = 0.f;
+#pragma unroll
+                for (int a = 0; a < CY; ++a) {
+                    wy[a] = axis_w<CY>(AY, sy, a, y);
+                    sum += wy[a];
+                }
+                const float inv = 1.0f / sum;
+#pragma unroll
+                for (int a = 0; a < CY; ++a) wy[a] *= inv;
+            } else {
+                wy[0] = 1.f;
+            }
+            float acc[VEC];
+#pragma unroll
+            for (int l = 0; l < VEC; ++l) acc[l] = 0.f;
+#pragma unroll
+            for (int a = 0; a < CY; ++a)
+#pragma unroll
+                for (int b = 0; b < CX; ++b) {
+                    float x[VEC];
+                    x_ab(a, b, x);
+#pragma unroll
+                    for (int l = 0; l < VEC; ++l) {
+                        const float wgt = CX > 1 ? wy[a] * wx[b][l] : wy[a];
+                        acc[l] = fmaf(wgt, x[l], acc[l]);
+                    }
+                }
+            return acc_pack<DT, VEC>(acc);
+        };
+        if constexpr (VEC * RElt<DT>::BYTES == 16) {
+            auto issue = [&](int m) {
+                const int y = AY.seg_start[sy] + r0 + m * bdy;
+                const uint32_t st = my_slot + (uint32_t)((m % S) * NU) * slot_stride;
+#pragma unroll
+                for (int n = 0; n < NU; ++n)
+                    cp_async16(st + (uint32_t)n * slot_stride, src[n] + (int64_t)y * pitch[n % CX]);
+            };
+#pragma unroll
+            for (int m = 0; m < S - 1; ++m) {
+                if (m < nrows) issue(m);
+                cp_async_commit();
+            }
+            for (int m = 0; m < nrows; ++m) {
+                if (m + S - 1 < nrows) issue(m + S - 1);
+                cp_async_commit();
+                cp_async_wait<S - 1>();
+                const int y = AY.seg_start[sy] + r0 + m * bdy;
+                const uint32_t st = my_slot + (uint32_t)((m % S) * NU) * slot_stride;
+                uint4 o;
+                if constexpr (NU == 1) {
+                    o = lds16(st);  // one tile: its normalised weight is exactly 1
+                } else {
+                    o = combine(y, [&](int a, int b, float (&x)[VEC]) {
+                        const uint4 v = lds16(st + (uint32_t)(a * CX + b) * slot_stride);
+                        unpack_chunk<DT, VEC>(v, x);
+                    });
+                }
+                __stcs(reinterpret_cast<uint4*>(dst + (int64_t)y * opitch), o);
+            }
+            cp_async_wait<0>();
+        } else {
+            // element path (unaligned geometry): plain loads, one row at a time
+            for (int m = 0; m < nrows; ++m) {
+                const int y = AY.seg_start[sy] + r0 + m * bdy;
+                if constexpr (NU == 1) {
+                    store_elem<DT>(dst + (int64_t)y * opitch, load_elem<DT>(src[0] + (int64_t)y * pitch[0]));
+                } else {
+                    const uint4 o = combine(y, [&](int a, int b, float (&x)[VEC]) {
+                        x[0] = elem_value<DT>(load_elem<DT>(src[a * CX + b] + (int64_t)y * pitch[b]));
+                    });
+                    store_elem<DT>(dst + (int64_t)y * opitch, o.x);
+                }
+            }
+        }
+    }
+}
+
+template <int DT, int VEC>
+__global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_constant__ RampParams p) {
+    extern __shared__ __align__(16) unsigned char s_ring[];
+    // blockIdx.x: (plane, rectangle) with the rectangle fastest; blockIdx.y:
+    // run of rows inside the rectangle
+    const int nrect = p.ay.nseg * p.ax.nseg;
+    const int rect = (int)(blockIdx.x % (unsigned)nrect);
+    const int64_t plane = blockIdx.x / (unsigned)nrect;
+    const int sy = rect / p.ax.nseg, sx = rect % p.ax.nseg;
+    const int rows = p.ay.seg_len[sy];
+    const int rbeg = blockIdx.y * p.rows_per_piece[sx];
+    if (rbeg >= rows) return;
+    const int rend = min(rows, rbeg + p.rows_per_piece[sx]);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint32_t ring = (uint32_t)__cvta_generic_to_shared(s_ring);
+    const int cy = p.ay.seg_n[sy], cx = p.ax.seg_n[sx];
+    switch (cy * 4 + cx) {
+        case 5: run_rect<1, 1, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        case 6: run_rect<1, 2, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        case 7: run_rect<1, 3, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        case 9: run_rect<2, 1, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        case 10: run_rect<2, 2, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        case 11: run_rect<2, 3, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        case 13: run_rect<3, 1, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        case 14: run_rect<3, 2, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        case 15: run_rect<3, 3, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        default: break;
+    }
+}
+
+}  // namespace
+
+int ramp_block() { return RAMP_BLOCK; }
+int ramp_smem() { return RAMP_SLOTS * RAMP_BLOCK * 16; }
+
+cudaError_t launch_ramp(const RampParams& p, int dtype, int vec, int grid_x, int grid_y, cudaStream_t s) {
+    void (*fn)(const RampParams);
+    switch (dtype) {
+        case F32: fn = vec > 1 ? ramp_kernel<F32, 4> : ramp_kernel<F32, 1>; break;
+        case F16: fn = vec > 1 ? ramp_kernel<F16, 8> : ramp_kernel<F16, 1>; break;
+        default: fn = vec > 1 ? ramp_kernel<BF16, 8> : ramp_kernel<BF16, 1>; break;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid_x, (unsigned)grid_y, 1);
+    cfg.blockDim = dim3(RAMP_BLOCK, 1, 1);
+    cfg.dynamicSmemBytes = vec > 1 ? (size_t)ramp_smem() : 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+}  // namespace tb

@@ -45,6 +45,11 @@ class tb_axis(ctypes.Structure):
                 ("scale", ctypes.c_int32), ("blend_extent", ctypes.c_int32), ("row_limit", ctypes.c_int32)]
 
 
+class tb_ramp_axis(ctypes.Structure):
+    _fields_ = [("n_tiles", ctypes.c_int32), ("tile_extent", ctypes.c_int32), ("out_extent", ctypes.c_int32),
+                ("zero", ctypes.c_int32), ("ramp", ctypes.c_int32), ("origins", ctypes.POINTER(ctypes.c_int64))]
+
+
 class tb_gn_partial(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("mean", ctypes.c_float), ("m2", ctypes.c_float)]
 
@@ -73,13 +78,17 @@ _lib.tb_patch_gn_apply.restype = ctypes.c_int
 _lib.tb_patch_gn_apply.argtypes = [_P_vp, _P_vp, _i32, ctypes.c_int, _i64, _i64, _P_i64, _i32, _vp, _vp, _vp,
                                    ctypes.c_float, _i32, _vp]
 
+_lib.tb_stitch2d_ramp.restype = ctypes.c_int
+_lib.tb_stitch2d_ramp.argtypes = [_P_vp, ctypes.c_int, _i64, _i64, ctypes.POINTER(tb_ramp_axis),
+                                  ctypes.POINTER(tb_ramp_axis), _vp, _vp]
 _lib.tb_patch_group_norm_noalloc.restype = ctypes.c_int
 _lib.tb_patch_group_norm_noalloc.argtypes = [_P_vp, _P_vp, _i32, ctypes.c_int, _i64, _i64, _P_i64, _i32, _vp, _vp,
                                              ctypes.c_float, _i32, _vp]
 TB_NOALLOC_MAX_PARTIALS = 65536
 
 EXPORTED = ("tb_version", "tb_status_string", "tb_last_cuda_error", "tb_axis_layout", "tb_stitch2d",
-            "tb_stitch3d", "tb_patch_gn_stats", "tb_patch_gn_apply", "tb_patch_group_norm_noalloc")
+            "tb_stitch3d", "tb_stitch2d_ramp", "tb_patch_gn_stats", "tb_patch_gn_apply",
+            "tb_patch_group_norm_noalloc")
 
 
 class TileBlendError(RuntimeError):
@@ -237,6 +246,62 @@ def tb_stitch2d_raw(tile_ptrs: Sequence[int], dtype: int, B: int, C: int, ay: Ax
     a_y, a_x = ay.c(), ax.c()
     _check(_lib.tb_stitch2d(_ptr_array(tile_ptrs), dtype, B, C, ctypes.byref(a_y), ctypes.byref(a_x), out_ptr,
                             H, W, _stream_handle(stream)), "tb_stitch2d")
+
+
+# ---------------------------------------------------------------------------
+# normalised-ramp stitch
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class RampAxis:
+    """One axis of a normalised-ramp tile layout (see tb_ramp_axis)."""
+    origins: Tuple[int, ...]   # output samples, ascending, first 0, last + tile_extent == out_extent
+    tile_extent: int
+    out_extent: int
+    zero: int                  # samples of zero weight next to a shared edge
+    ramp: int                  # samples over which the weight rises to 1
+
+    @staticmethod
+    def spread(latent_extent: int, latent_tile: int, n_tiles: int, scale: int, zero_latents: int = 4,
+               ramp_latents: int = 8) -> "RampAxis":
+        """n_tiles tiles spread so the first starts at 0 and the last ends at
+        the edge: tile n at floor(n * (latent_extent - latent_tile) /
+        (n_tiles - 1)) latents."""
+        span = latent_extent - latent_tile
+        org = tuple(0 if n_tiles == 1 else (n * span // (n_tiles - 1)) * scale for n in range(n_tiles))
+        return RampAxis(org, latent_tile * scale, latent_extent * scale, zero_latents * scale, ramp_latents * scale)
+
+    def c(self):
+        arr = (ctypes.c_int64 * len(self.origins))(*self.origins)
+        st = tb_ramp_axis(len(self.origins), self.tile_extent, self.out_extent, self.zero, self.ramp,
+                          ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64)))
+        st._keep = arr  # the struct points into this array
+        return st
+
+
+def tb_stitch2d_ramp(tiles: Sequence[Sequence[torch.Tensor]], ay: RampAxis, ax: RampAxis, out: torch.Tensor,
+                     stream=None) -> torch.Tensor:
+    """Normalised-ramp stitch of ``tiles[i][j]`` ([B, C, ay.tile_extent,
+    ax.tile_extent]) into ``out`` ([B, C, ay.out_extent, ax.out_extent])."""
+    _cuda_contig(out, "out")
+    B, C, H, W = out.shape
+    if (H, W) != (ay.out_extent, ax.out_extent):
+        raise ValueError("out must be [B, C, %d, %d]" % (ay.out_extent, ax.out_extent))
+    if len(tiles) != len(ay.origins) or any(len(r) != len(ax.origins) for r in tiles):
+        raise ValueError("expected a %d x %d tile grid" % (len(ay.origins), len(ax.origins)))
+    shape = (B, C, ay.tile_extent, ax.tile_extent)
+    ptrs = []
+    for i, row in enumerate(tiles):
+        for j, t in enumerate(row):
+            if t.dtype != out.dtype or t.shape != shape or not t.is_cuda or not t.is_contiguous():
+                _cuda_contig(t, "tile (%d,%d)" % (i, j))
+                raise ValueError("tile (%d,%d) has %s %s, expected %s %s" % (i, j, t.dtype, tuple(t.shape),
+                                                                            out.dtype, shape))
+            ptrs.append(t.data_ptr())
+    a_y, a_x = ay.c(), ax.c()
+    _check(_lib.tb_stitch2d_ramp(_ptr_array(ptrs), _dtype_code(out), B, C, ctypes.byref(a_y), ctypes.byref(a_x),
+                                 out.data_ptr(), _stream_handle(stream)), "tb_stitch2d_ramp")
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -63,6 +63,33 @@ STITCH = {
 
 
 @dataclass(frozen=True)
+class RampWorkload:
+    """Equally sized tiles spread over the canvas (first at 0, last at the
+    edge), blended with the normalised ramp: zero weight for 4 latents next
+    to a shared edge, full weight 8 latents later."""
+    name: str
+    dtype: str
+    B: int
+    C: int
+    latent_hw: Tuple[int, int]
+    latent_tile: int
+    n_tiles: Tuple[int, int]
+    scale: int
+    recipe: str
+    seed: int
+
+
+RAMP = {
+    # decoded tiles: 2048x2048 (256 latents at 8x), 64-latent tiles, 16-latent overlaps
+    "ramp_2048_bf16": RampWorkload("ramp_2048_bf16", "bf16", 1, 3, (256, 256), 64, (5, 5), 8, "smooth", 1240),
+    # latent-space tiles of a tiled encode: batch 4, 16 channels, 256x256 latents (a 2048 px image at 8x),
+    # 64-latent tiles with 32-latent overlaps
+    "ramp_latent_256_bf16": RampWorkload("ramp_latent_256_bf16", "bf16", 4, 16, (256, 256), 64, (7, 7), 1,
+                                         "smooth", 1241),
+}
+
+
+@dataclass(frozen=True)
 class GroupNormWorkload:
     name: str
     dtype: str
@@ -96,3 +123,11 @@ def make_stitch_tiles(w: StitchWorkload, boxes: Sequence[Sequence[Tuple[int, int
 
 def make_groupnorm_inputs(w: GroupNormWorkload):
     return synth.groupnorm_patches(w.seed, w.shape, w.split_dim, w.patches, w.patch_means, w.dtype)
+
+
+def make_ramp_tiles(w: RampWorkload, ay, ax):
+    """CPU tiles of a ramp workload cut from one smooth field; ``ay`` / ``ax``
+    carry the tile origins and extents (samples)."""
+    return synth.smooth_field_tiles(w.seed, w.B, w.C, (ay.out_extent, ax.out_extent),
+                                    [(o, ay.tile_extent) for o in ay.origins],
+                                    [(o, ax.tile_extent) for o in ax.origins], w.dtype)

@@ -163,3 +163,28 @@ def test_status_strings(tbl):
     for s in range(7):
         assert tbl._lib.tb_status_string(s)
     assert tbl._lib.tb_status_string(99) == b"unknown status"
+
+
+def test_ramp_stitch_rejects_bad_layouts_before_launch(tbl):
+    def call(ay, ax, dtype=2):
+        arr = (ctypes.c_void_p * 64)(*([16] * 64))
+        a, b = ay.c(), ax.c()
+        return tbl._lib.tb_stitch2d_ramp(arr, dtype, 1, 3, ctypes.byref(a), ctypes.byref(b), 16, None)
+    good = tbl.RampAxis.spread(256, 64, 5, 8)
+    assert good.origins == (0, 384, 768, 1152, 1536)
+    assert call(good, good, dtype=5) == tbl.TB_ERR_DTYPE
+    # last tile not ending at the canvas edge
+    assert call(tbl.RampAxis((0, 384), 512, 1024, 32, 64), good) == tbl.TB_ERR_GEOMETRY
+    # origins out of order
+    assert call(tbl.RampAxis((0, 600, 512), 512, 1024, 32, 64), good) == tbl.TB_ERR_GEOMETRY
+    # overlap shorter than the zero bands: the seam has no weight
+    assert call(tbl.RampAxis((0, 500), 512, 1012, 32, 64), good) == tbl.TB_ERR_GEOMETRY
+    # ramp of zero samples
+    assert call(tbl.RampAxis((0, 384), 512, 896, 32, 0), good) == tbl.TB_ERR_GEOMETRY
+    # four tiles with positive weight at one position
+    dense = tbl.RampAxis(tuple(range(0, 97, 8)), 64, 160, 0, 1)
+    assert call(dense, good) == tbl.TB_ERR_UNSUPPORTED
+    # nothing to do
+    arr = (ctypes.c_void_p * 64)()
+    a, b = good.c(), good.c()
+    assert tbl._lib.tb_stitch2d_ramp(arr, 2, 0, 3, ctypes.byref(a), ctypes.byref(b), None, None) == tbl.TB_OK
