@@ -203,7 +203,7 @@ typedef struct {
 } tb_ramp_axis;
 
 /* Most tiles with positive weight at one position of a ramp axis. */
-#define TB_RAMP_MAX_COVER 4
+#define TB_RAMP_MAX_COVER 3
 
 /*
  * tb_stitch2d_ramp -- stitch a 2D grid of equally sized overlapping tiles by

@@ -37,6 +37,8 @@
 #define TB_GN_FORCE_CS 0
 #endif
 
+static_assert(tb::RAMP_MAXCOVER == TB_RAMP_MAX_COVER, "ramp cover limit differs from the header");
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
