@@ -16,4 +16,8 @@ rounding   IEEE round-to-nearest-even into fp16 / bf16, from the same C file.
 groupnorm  the unsharded GroupNorm (+ SiLU) in float64 numpy, and the two
            broken PatchGroupNorm variants described on the DistVAE page, kept
            as negative controls.
+ramp       the normalised-ramp stitch of equally sized tiles, in float64.
+patchify   the ragged band split of one axis among ranks (whole bands of
+           the VAE's scale factor, the first ranks one band more) and the
+           gather that reassembles the patches, in plain numpy.
 """
