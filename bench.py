@@ -481,6 +481,22 @@ def per_kernel(torch, tb, W, dev, peak, reps):
               2 * elems * es, "gn_apply", name)
         del sets
         torch.cuda.empty_cache()
+    for name, w in W.PATCHIFY.items():
+        x = W.make_patchify_input(w)
+        nbytes = 2 * x.numel() * x.element_size()     # every element read once and written once
+        _, sizes = tb.tb_patchify_layout(w.shape[w.axis], w.factor, w.ranks)
+        ns = nsets_for(nbytes)
+        sets = []
+        for _ in range(ns):
+            xd = x.to(dev)
+            parts = tb.tb_patchify(xd, w.axis, w.factor, w.ranks)
+            sets.append((xd, parts, torch.empty_like(xd)))
+        timed(lambda q: tb.tb_patchify(sets[q][0], w.axis, w.factor, w.ranks, patches=sets[q][1]), ns, nbytes,
+              "patchify", name)
+        timed(lambda q: tb.tb_gather_patches(sets[q][1], sizes, w.axis, out=sets[q][2]), ns, nbytes,
+              "gather_patches", name)
+        del sets
+        torch.cuda.empty_cache()
     return res
 
 
@@ -507,6 +523,24 @@ def run_profile_target(args):
         else:
             dt = [[[t.to(dev) for t in row] for row in pl] for pl in tiles]
             launch = lambda: tb.tb_stitch3d(dt, axes[0], axes[1], axes[2], out)
+    elif kernel == "stitch2d_ramp":
+        w = W.RAMP[name]
+        ay = tb.RampAxis.spread(w.latent_hw[0], w.latent_tile, w.n_tiles[0], w.scale)
+        ax = tb.RampAxis.spread(w.latent_hw[1], w.latent_tile, w.n_tiles[1], w.scale)
+        dt = [[t.to(dev) for t in row] for row in W.make_ramp_tiles(w, ay, ax)]
+        tdt = dt[0][0].dtype
+        out = torch.empty((w.B, w.C, ay.out_extent, ax.out_extent), dtype=tdt, device=dev)
+        launch = lambda: tb.tb_stitch2d_ramp(dt, ay, ax, out)
+    elif kernel in ("patchify", "gather_patches"):
+        w = W.PATCHIFY[name]
+        xd = W.make_patchify_input(w).to(dev)
+        parts = tb.tb_patchify(xd, w.axis, w.factor, w.ranks)
+        back = torch.empty_like(xd)
+        sizes = [p.shape[w.axis] for p in parts]
+        if kernel == "patchify":
+            launch = lambda: tb.tb_patchify(xd, w.axis, w.factor, w.ranks, patches=parts)
+        else:
+            launch = lambda: tb.tb_gather_patches(parts, sizes, w.axis, out=back)
     else:
         w = W.GROUPNORM[name]
         patches, gamma, beta = W.make_groupnorm_inputs(w)

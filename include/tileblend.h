@@ -8,7 +8,8 @@
  *   [STU] "Studio: size seam-free VAE tiles from measured peaks" (unsloth PR
  *         #12764), commit "Decode this VAE in 32-latent tiles ...".
  *   [DVA] "Add tiled VAE parallelism & extended model support" (xDiT
- *         DistVAE PR #14), the PatchGroupNorm commits.
+ *         DistVAE PR #14), the PatchGroupNorm commits and the commits on
+ *         Patchify's ragged bands and on gather_patches.
  *
  * Conventions shared by every call
  *   - Plain C types only.  Device pointers point to memory the caller
@@ -272,6 +273,71 @@ tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dtype dtyp
 tb_status tb_patch_gn_apply(const void* const* patches, void* const* outs, int32_t P, tb_dtype dtype, int64_t N,
                             int64_t C, const int64_t* spatial, int32_t G, const tb_gn_partial* partials,
                             const void* gamma, const void* beta, float eps, int32_t silu, void* stream);
+
+/* Most patches (ranks) one Patchify split or patch gather handles. */
+#define TB_MAX_PATCHES 64
+
+/*
+ * tb_patchify_layout -- the ranks' bands of one axis (host only, no GPU)
+ * [DVA], Patchify: the axis is cut into bands of `factor` positions (the
+ * factor by which the VAE narrows or widens it), the bands are shared out
+ * in rank order as evenly as they go, and when they do not divide evenly the
+ * first ranks get one band more.  No position is invented or dropped.
+ *   extent   positions along the axis; a whole number of bands (>= 0)
+ *   factor   positions per band (>= 1)
+ *   P        ranks (1 .. TB_MAX_PATCHES)
+ *   starts   out, may be NULL: P offsets of the bands along the axis
+ *   sizes    out, may be NULL: P band extents (multiples of factor; 0 for
+ *            ranks past the band count)
+ * Errors: TB_ERR_SHAPE (extent < 0, factor < 1, P < 1, extent not a
+ * multiple of factor), TB_ERR_UNSUPPORTED (P > TB_MAX_PATCHES).
+ */
+tb_status tb_patchify_layout(int64_t extent, int32_t factor, int32_t P, int64_t* starts, int64_t* sizes);
+
+/*
+ * tb_patchify -- cut a tensor into the P ranks' patches along `axis` by the
+ * bands of tb_patchify_layout [DVA], one device copy for all of them.
+ *
+ *   x        device pointer, dense row-major tensor of `shape`
+ *   dtype    element type (only its size matters: the copy is bit exact)
+ *   ndim     1 .. 8;  shape: host array of ndim extents (>= 0)
+ *   axis     0 .. ndim-1, the split axis; shape[axis] must be a whole
+ *            number of bands
+ *   factor   band extent (>= 1);  P: ranks (1 .. TB_MAX_PATCHES)
+ *   slot     0: patch p is the dense tensor of `shape` with shape[axis]
+ *            replaced by sizes[p].  > 0: every patch buffer holds `slot`
+ *            positions along the axis (slot >= the largest band), as the
+ *            equal-shape buffers of a collective all-gather; band p fills
+ *            the first sizes[p] of them and the rest are left untouched
+ *   patches  host array of P device pointers (a pointer of an empty patch
+ *            may be NULL); no patch may overlap x or another patch
+ * Errors: TB_ERR_NULL, TB_ERR_DTYPE, TB_ERR_SHAPE (ndim, axis, negative
+ * extents, a partial band, 0 < slot < largest band, slot < 0),
+ * TB_ERR_UNSUPPORTED (P > TB_MAX_PATCHES, more than 2^31 - 1 rows before
+ * the axis or elements in one row of a patch), TB_ERR_CUDA.
+ */
+tb_status tb_patchify(const void* x, tb_dtype dtype, int32_t ndim, const int64_t* shape, int32_t axis,
+                      int32_t factor, int32_t P, int64_t slot, void* const* patches, void* stream);
+
+/*
+ * tb_gather_patches -- reassemble the tensor from the P ranks' patches
+ * [DVA], gather_patches: the sizes along `axis` are given (the exchange
+ * of sizes that comes first on the page), each patch is read without its
+ * padding, and the patches are concatenated in rank order.  One device copy.
+ *
+ *   patches  host array of P device pointers (NULL allowed for size 0)
+ *   P        1 .. TB_MAX_PATCHES
+ *   sizes    host array of P extents along the axis (>= 0), summing to
+ *            shape[axis]; any sizes, not only tb_patchify_layout's
+ *   dtype, ndim, axis   as tb_patchify; shape: the gathered tensor
+ *   slot     0: dense patches; > 0: every patch buffer has `slot`
+ *            positions along the axis and only the first sizes[p] are read
+ *   out      device pointer to the gathered tensor; must not overlap a patch
+ * Errors as tb_patchify (TB_ERR_SHAPE also when the sizes do not sum to
+ * shape[axis]).
+ */
+tb_status tb_gather_patches(const void* const* patches, int32_t P, const int64_t* sizes, tb_dtype dtype, int32_t ndim,
+                            const int64_t* shape, int32_t axis, int64_t slot, void* out, void* stream);
 
 /*
  * tb_patch_group_norm_noalloc -- PatchGroupNorm (statistics, then pooled

@@ -27,6 +27,7 @@ UNITS = {
     "tb_groupnorm.cu": [],
     "tb_noalloc.cu": [],
     "tb_ramp.cu": [],
+    "tb_patchify.cu": [],
 }
 HEADERS = ["tb_internal.h"]
 

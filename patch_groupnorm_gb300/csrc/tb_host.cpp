@@ -313,6 +313,100 @@ tb_status gn_validate(const void* const* patches, int32_t P, tb_dtype dtype, int
     return TB_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Patchify split / patch gather
+// ---------------------------------------------------------------------------
+
+tb_status band_layout(int64_t extent, int32_t factor, int32_t P, int64_t* starts, int64_t* sizes) {
+    if (extent < 0 || factor < 1 || P < 1) return TB_ERR_SHAPE;
+    if (extent % factor != 0) return TB_ERR_SHAPE;
+    if (P > tb::PF_MAXP) return TB_ERR_UNSUPPORTED;
+    const int64_t bands = extent / factor, each = bands / P, extra = bands % P;
+    int64_t at = 0;
+    for (int p = 0; p < P; ++p) {
+        const int64_t size = (each + (p < extra ? 1 : 0)) * factor;
+        if (starts) starts[p] = at;
+        if (sizes) sizes[p] = size;
+        at += size;
+    }
+    return TB_OK;
+}
+
+// The tensor of `shape` seen as [outer, extent, inner] around `axis`.
+tb_status split_view(int32_t ndim, const int64_t* shape, int32_t axis, int64_t& outer, int64_t& extent,
+                     int64_t& inner) {
+    if (shape == nullptr) return TB_ERR_NULL;
+    if (ndim < 1 || ndim > 8 || axis < 0 || axis >= ndim) return TB_ERR_SHAPE;
+    double total = 1.0;
+    outer = 1;
+    inner = 1;
+    for (int d = 0; d < ndim; ++d) {
+        if (shape[d] < 0) return TB_ERR_SHAPE;
+        total *= (double)shape[d];
+        if (d < axis) outer *= shape[d];
+        if (d > axis) inner *= shape[d];
+        if (total > 1.0e18) return TB_ERR_SHAPE;
+    }
+    extent = shape[axis];
+    return TB_OK;
+}
+
+// One launch copying the P bands between the whole tensor and the patches.
+tb_status patch_copy(bool to_patches, void* whole, void* const* patches, int32_t P, const int64_t* starts,
+                     const int64_t* sizes, int eb, int64_t outer, int64_t extent, int64_t inner, int64_t slot,
+                     void* stream) {
+    int64_t largest = 0;
+    for (int p = 0; p < P; ++p) largest = std::max(largest, sizes[p]);
+    if (slot < 0 || (slot > 0 && slot < largest)) return TB_ERR_SHAPE;
+    if (outer == 0 || inner == 0 || extent == 0) return TB_OK;
+    if (whole == nullptr) return TB_ERR_NULL;
+    for (int p = 0; p < P; ++p)
+        if (sizes[p] > 0 && patches[p] == nullptr) return TB_ERR_NULL;
+    // widest chunk dividing every run, pitch, offset and base address
+    int vec = 16;
+    auto fit = [&vec](uint64_t q) {
+        while (vec > 1 && q % (uint64_t)vec != 0) vec >>= 1;
+    };
+    fit((uint64_t)(extent * inner * eb));
+    fit((uint64_t)reinterpret_cast<uintptr_t>(whole));
+    for (int p = 0; p < P; ++p) {
+        if (sizes[p] == 0) continue;
+        fit((uint64_t)(sizes[p] * inner * eb));
+        fit((uint64_t)(starts[p] * inner * eb));
+        fit((uint64_t)((slot > 0 ? slot : sizes[p]) * inner * eb));
+        fit((uint64_t)reinterpret_cast<uintptr_t>(patches[p]));
+    }
+    // element counts in chunks (a chunk narrower than an element only for
+    // a base address that is not aligned to the element)
+    auto chunks = [&](int64_t elems) { return elems * eb / vec; };
+    if (outer + tb::PF_BLOCK >= 2147483647LL) return TB_ERR_UNSUPPORTED;
+    tb::PatchCopyParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.whole = whole;
+    prm.wpitch = chunks(extent * inner);
+    prm.P = P;
+    const int64_t cta_chunks = tb::PF_CTA_BYTES / vec;
+    int64_t ranges = 1;
+    for (int p = 0; p < P; ++p) {
+        const int64_t run = chunks(sizes[p] * inner);
+        if (run >= 2147483647LL) return TB_ERR_UNSUPPORTED;
+        prm.patch[p] = patches[p];
+        prm.n[p] = outer * run;
+        prm.run[p] = (int32_t)std::max<int64_t>(run, 1);
+        prm.step_o[p] = tb::PF_BLOCK / prm.run[p];
+        prm.step_r[p] = tb::PF_BLOCK % prm.run[p];
+        prm.woff[p] = chunks(starts[p] * inner);
+        prm.ppitch[p] = chunks((slot > 0 ? slot : sizes[p]) * inner);
+        ranges = std::max(ranges, (prm.n[p] + cta_chunks - 1) / cta_chunks);
+    }
+    for (int p = 0; p < P; ++p) prm.per_cta[p] = std::max<int64_t>(1, (prm.n[p] + ranges - 1) / ranges);
+    const int64_t grid = ranges * P;
+    if (grid > 2147483647LL) return TB_ERR_UNSUPPORTED;
+    cudaError_t e = tb::launch_patch_copy(prm, vec, to_patches, grid, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return TB_OK;
+}
+
 }  // namespace
 
 void tb::record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
@@ -587,4 +681,43 @@ TB_API tb_status tb_patch_gn_apply(const void* const* patches, void* const* outs
     cudaError_t e = tb::launch_gn_apply(prm, (int)dtype, items, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return TB_OK;
+}
+
+TB_API tb_status tb_patchify_layout(int64_t extent, int32_t factor, int32_t P, int64_t* starts, int64_t* sizes) {
+    return band_layout(extent, factor, P, starts, sizes);
+}
+
+TB_API tb_status tb_patchify(const void* x, tb_dtype dtype, int32_t ndim, const int64_t* shape, int32_t axis,
+                             int32_t factor, int32_t P, int64_t slot, void* const* patches, void* stream) {
+    if (dtype != TB_F32 && dtype != TB_F16 && dtype != TB_BF16) return TB_ERR_DTYPE;
+    int64_t outer, extent, inner;
+    tb_status s = split_view(ndim, shape, axis, outer, extent, inner);
+    if (s != TB_OK) return s;
+    int64_t starts[tb::PF_MAXP], sizes[tb::PF_MAXP];
+    s = band_layout(extent, factor, P, starts, sizes);
+    if (s != TB_OK) return s;
+    if (patches == nullptr) return TB_ERR_NULL;
+    return patch_copy(true, const_cast<void*>(x), patches, P, starts, sizes, elem_bytes(dtype), outer, extent, inner,
+                      slot, stream);
+}
+
+TB_API tb_status tb_gather_patches(const void* const* patches, int32_t P, const int64_t* sizes, tb_dtype dtype,
+                                   int32_t ndim, const int64_t* shape, int32_t axis, int64_t slot, void* out,
+                                   void* stream) {
+    if (dtype != TB_F32 && dtype != TB_F16 && dtype != TB_BF16) return TB_ERR_DTYPE;
+    int64_t outer, extent, inner;
+    tb_status s = split_view(ndim, shape, axis, outer, extent, inner);
+    if (s != TB_OK) return s;
+    if (P < 1) return TB_ERR_SHAPE;
+    if (P > tb::PF_MAXP) return TB_ERR_UNSUPPORTED;
+    if (sizes == nullptr || patches == nullptr) return TB_ERR_NULL;
+    int64_t starts[tb::PF_MAXP], at = 0;
+    for (int p = 0; p < P; ++p) {
+        if (sizes[p] < 0 || sizes[p] > extent - at) return TB_ERR_SHAPE;
+        starts[p] = at;
+        at += sizes[p];
+    }
+    if (at != extent) return TB_ERR_SHAPE;
+    return patch_copy(false, out, const_cast<void* const*>(patches), P, starts, sizes, elem_bytes(dtype), outer, extent,
+                      inner, slot, stream);
 }

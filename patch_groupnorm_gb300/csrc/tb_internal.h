@@ -155,6 +155,38 @@ int ramp_smem();
 cudaError_t launch_ramp(const RampParams& p, int dtype, int vec, int grid_x, int grid_y, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
+// Patchify split / patch gather
+// ---------------------------------------------------------------------------
+
+constexpr int PF_MAXP = 64;
+constexpr int PF_BLOCK = 256;          // threads per CTA
+constexpr int PF_CTA_BYTES = 32768;    // bytes one CTA moves at most
+
+// The whole tensor viewed as [outer, extent, inner]; patch p holds rows
+// [start_p, start_p + size_p) of every outer slice.  All offsets below are
+// in chunks of `vec` bytes (a power of two that divides every run, pitch,
+// offset and base address).  Position (o, r) of patch p -- outer slice o,
+// chunk r of its run -- is chunk o * ppitch[p] + r of the patch buffer and
+// chunk o * wpitch + woff[p] + r of the whole tensor.
+struct PatchCopyParams {
+    void* patch[PF_MAXP];
+    void* whole;
+    int64_t n[PF_MAXP];        // chunks of patch p: outer * run[p]
+    int64_t per_cta[PF_MAXP];  // chunks one CTA of patch p copies
+    int64_t woff[PF_MAXP];     // run start inside an outer slice of the whole
+    int64_t ppitch[PF_MAXP];   // chunks per outer slice of the patch buffer
+    int32_t run[PF_MAXP];      // chunks per outer slice of band p (>= 1 if n > 0)
+    int32_t step_o[PF_MAXP];   // PF_BLOCK / run[p]
+    int32_t step_r[PF_MAXP];   // PF_BLOCK % run[p]
+    int64_t wpitch;            // chunks per outer slice of the whole
+    int32_t P;
+};
+static_assert(sizeof(PatchCopyParams) <= 32000, "kernel parameter block too large");
+
+// to_patches: whole -> patches (the split), else patches -> whole (the gather).
+cudaError_t launch_patch_copy(const PatchCopyParams& p, int vec, bool to_patches, int64_t grid, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // PatchGroupNorm
 // ---------------------------------------------------------------------------
 

@@ -17,6 +17,7 @@ Recipes (decoded VAE tiles and decoder activations stand in for real ones):
   (t, y, x), temporal frequency U(0.5, 4) cycles per clip.
 * GroupNorm patches: patch p ~ N(mu_p, 1), gamma ~ N(1, 0.1^2),
   beta ~ N(0, 0.1^2).
+* activation: one tensor of i.i.d. N(0, 1) (the input of a patch split).
 """
 import math
 from typing import List, Sequence, Tuple
@@ -136,3 +137,9 @@ def groupnorm_patches(seed: int, full_shape: Sequence[int], split_dim: int, n_pa
     gamma = (1.0 + 0.1 * torch.randn(C, generator=g, dtype=torch.float64)).to(TORCH_DTYPES[dtype])
     beta = (0.1 * torch.randn(C, generator=g, dtype=torch.float64)).to(TORCH_DTYPES[dtype])
     return patches, gamma, beta
+
+
+def normal_tensor(seed: int, shape: Sequence[int], dtype: str) -> torch.Tensor:
+    """i.i.d. N(0, 1) of ``shape``, drawn in float32 and cast."""
+    g = _gen(seed)
+    return torch.randn(list(shape), generator=g, dtype=torch.float32).to(TORCH_DTYPES[dtype]).contiguous()

@@ -85,10 +85,17 @@ _lib.tb_patch_group_norm_noalloc.restype = ctypes.c_int
 _lib.tb_patch_group_norm_noalloc.argtypes = [_P_vp, _P_vp, _i32, ctypes.c_int, _i64, _i64, _P_i64, _i32, _vp, _vp,
                                              ctypes.c_float, _i32, _vp]
 TB_NOALLOC_MAX_PARTIALS = 65536
+_lib.tb_patchify_layout.restype = ctypes.c_int
+_lib.tb_patchify_layout.argtypes = [_i64, _i32, _i32, _P_i64, _P_i64]
+_lib.tb_patchify.restype = ctypes.c_int
+_lib.tb_patchify.argtypes = [_vp, ctypes.c_int, _i32, _P_i64, _i32, _i32, _i32, _i64, _P_vp, _vp]
+_lib.tb_gather_patches.restype = ctypes.c_int
+_lib.tb_gather_patches.argtypes = [_P_vp, _i32, _P_i64, ctypes.c_int, _i32, _P_i64, _i32, _i64, _vp, _vp]
+TB_MAX_PATCHES = 64
 
 EXPORTED = ("tb_version", "tb_status_string", "tb_last_cuda_error", "tb_axis_layout", "tb_stitch2d",
             "tb_stitch3d", "tb_stitch2d_ramp", "tb_patch_gn_stats", "tb_patch_gn_apply",
-            "tb_patch_group_norm_noalloc")
+            "tb_patch_group_norm_noalloc", "tb_patchify_layout", "tb_patchify", "tb_gather_patches")
 
 
 class TileBlendError(RuntimeError):
@@ -420,3 +427,74 @@ def tb_patch_group_norm_noalloc(patches: Sequence[torch.Tensor], outs: Sequence[
                                             1 if silu else 0, _stream_handle(stream)),
            "tb_patch_group_norm_noalloc")
     return outs
+
+
+# ---------------------------------------------------------------------------
+# Patchify split / patch gather
+# ---------------------------------------------------------------------------
+
+def tb_patchify_layout(extent: int, factor: int, P: int) -> Tuple[List[int], List[int]]:
+    """(starts, sizes) of the P ranks' bands of an axis of ``extent``
+    positions: whole bands of ``factor``, the first ranks one band more."""
+    starts, sizes = (ctypes.c_int64 * max(1, P))(), (ctypes.c_int64 * max(1, P))()
+    _check(_lib.tb_patchify_layout(extent, factor, P, starts, sizes), "tb_patchify_layout")
+    return list(starts[:P]), list(sizes[:P])
+
+
+def _shape_arr(shape) -> ctypes.Array:
+    return (ctypes.c_int64 * max(1, len(shape)))(*shape)
+
+
+def tb_patchify(x: torch.Tensor, axis: int, factor: int, P: int, patches: Optional[Sequence[torch.Tensor]] = None,
+                slot: int = 0, stream=None) -> List[torch.Tensor]:
+    """The P ranks' patches of ``x`` along ``axis``.  With ``slot`` > 0 every
+    patch buffer has ``slot`` positions along the axis (the band fills the
+    first ones; the rest are not written)."""
+    _cuda_contig(x, "x")
+    axis = axis % x.dim()
+    _, sizes = tb_patchify_layout(x.shape[axis], factor, P)
+    shapes = []
+    for sz in sizes:
+        sh = list(x.shape)
+        sh[axis] = slot if slot > 0 else sz
+        shapes.append(tuple(sh))
+    if patches is None:
+        patches = [torch.empty(sh, dtype=x.dtype, device=x.device) for sh in shapes]
+    if len(patches) != P:
+        raise ValueError("one patch buffer per rank")
+    for q, (t, sh) in enumerate(zip(patches, shapes)):
+        _cuda_contig(t, "patch %d" % q)
+        if tuple(t.shape) != sh or t.dtype != x.dtype:
+            raise ValueError("patch %d must be %s %s" % (q, x.dtype, sh))
+    _check(_lib.tb_patchify(x.data_ptr(), _dtype_code(x), x.dim(), _shape_arr(x.shape), axis, factor, P, slot,
+                            _ptr_array([t.data_ptr() for t in patches]), _stream_handle(stream)), "tb_patchify")
+    return list(patches)
+
+
+def tb_gather_patches(patches: Sequence[torch.Tensor], sizes: Sequence[int], axis: int,
+                      out: Optional[torch.Tensor] = None, slot: int = 0, stream=None) -> torch.Tensor:
+    """Concatenate the first ``sizes[p]`` positions along ``axis`` of every
+    patch, in rank order.  With ``slot`` > 0 every patch buffer has ``slot``
+    positions along the axis."""
+    if len(patches) == 0 or len(sizes) != len(patches):
+        raise ValueError("one size per patch, at least one patch")
+    ref = patches[0]
+    axis = axis % ref.dim()
+    shape = list(ref.shape)
+    shape[axis] = sum(sizes)
+    for q, (t, sz) in enumerate(zip(patches, sizes)):
+        _cuda_contig(t, "patch %d" % q)
+        want = list(ref.shape)
+        want[axis] = slot if slot > 0 else sz
+        if list(t.shape) != want or t.dtype != ref.dtype:
+            raise ValueError("patch %d must be %s %s" % (q, ref.dtype, tuple(want)))
+    if out is None:
+        out = torch.empty(shape, dtype=ref.dtype, device=ref.device)
+    _cuda_contig(out, "out")
+    if list(out.shape) != shape or out.dtype != ref.dtype:
+        raise ValueError("out must be %s %s" % (ref.dtype, tuple(shape)))
+    sz = (ctypes.c_int64 * len(sizes))(*sizes)
+    _check(_lib.tb_gather_patches(_ptr_array([t.data_ptr() for t in patches]), len(patches), sz, _dtype_code(out),
+                                  out.dim(), _shape_arr(shape), axis, slot, out.data_ptr(), _stream_handle(stream)),
+           "tb_gather_patches")
+    return out

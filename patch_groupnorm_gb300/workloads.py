@@ -3,7 +3,8 @@
 Each stitch workload is a decoded image or clip cut into overlapping tiles by
 the stock tiled-decode rule (latent tile, overlap factor, latent scale); the
 tiles are drawn by ``synth``.  The PatchGroupNorm workloads are decoder
-activations split into four patches along one spatial axis.
+activations split into four patches along one spatial axis; the Patchify
+workloads split such activations among ranks and gather them back.
 
 The generator needs each tile's placement (output-space origin, extent);
 callers pass it from a derived geometry -- ``tileblend.tb_axis_layout`` in
@@ -110,6 +111,29 @@ GROUPNORM = {
 }
 
 
+@dataclass(frozen=True)
+class PatchifyWorkload:
+    """An activation split among ranks along one axis in whole bands of
+    ``factor`` positions (the first ranks one band more), and gathered back."""
+    name: str
+    dtype: str
+    shape: Tuple[int, ...]
+    axis: int
+    factor: int
+    ranks: int
+    seed: int
+
+
+PATCHIFY = {
+    # the 4D decoder activation of the GroupNorm workload, 4 ranks along the height: 64 rows each
+    "patchify_4d_1x512x256x256_h4": PatchifyWorkload("patchify_4d_1x512x256x256_h4", "bf16", (1, 512, 256, 256),
+                                                     2, 8, 4, 1242),
+    # the 5D activation, 3 ranks along the width: 26 bands of 8 -> 72, 72, 64 columns
+    "patchify_5d_1x384x13x120x208_w3": PatchifyWorkload("patchify_5d_1x384x13x120x208_w3", "bf16",
+                                                        (1, 384, 13, 120, 208), 4, 8, 3, 1243),
+}
+
+
 def make_stitch_tiles(w: StitchWorkload, boxes: Sequence[Sequence[Tuple[int, int]]], out_extents: Sequence[int]):
     """CPU tiles of workload ``w``; ``boxes[a]`` lists (origin, extent) of the
     tiles along axis a and ``out_extents`` the output extents."""
@@ -131,3 +155,7 @@ def make_ramp_tiles(w: RampWorkload, ay, ax):
     return synth.smooth_field_tiles(w.seed, w.B, w.C, (ay.out_extent, ax.out_extent),
                                     [(o, ay.tile_extent) for o in ay.origins],
                                     [(o, ax.tile_extent) for o in ax.origins], w.dtype)
+
+
+def make_patchify_input(w: PatchifyWorkload):
+    return synth.normal_tensor(w.seed, w.shape, w.dtype)

@@ -188,3 +188,60 @@ def test_ramp_stitch_rejects_bad_layouts_before_launch(tbl):
     arr = (ctypes.c_void_p * 64)()
     a, b = good.c(), good.c()
     assert tbl._lib.tb_stitch2d_ramp(arr, 2, 0, 3, ctypes.byref(a), ctypes.byref(b), None, None) == tbl.TB_OK
+
+
+def test_patchify_layout_matches_the_oracle(tbl):
+    from oracle.patchify import layout
+    rnd = random.Random(11)
+    for _ in range(2000):
+        factor = rnd.choice([1, 2, 4, 8, 16])
+        P = rnd.randint(1, tbl.TB_MAX_PATCHES)
+        extent = factor * rnd.randint(0, 300)
+        assert tbl.tb_patchify_layout(extent, factor, P) == tuple(map(list, layout(extent, factor, P)))
+
+
+def test_patchify_layout_rejects_bad_counts(tbl):
+    for args, st in (((209, 8, 3), tbl.TB_ERR_SHAPE), ((16, 0, 2), tbl.TB_ERR_SHAPE), ((16, 1, 0), tbl.TB_ERR_SHAPE),
+                     ((-8, 8, 2), tbl.TB_ERR_SHAPE), ((64, 1, 65), tbl.TB_ERR_UNSUPPORTED)):
+        with pytest.raises(tbl.TileBlendError) as e:
+            tbl.tb_patchify_layout(*args)
+        assert e.value.status == st
+
+
+def test_patchify_and_gather_reject_before_launch(tbl):
+    shape = (ctypes.c_int64 * 5)(1, 384, 13, 120, 208)
+    ptrs = (ctypes.c_void_p * 3)(16, 32, 48)
+    split = tbl._lib.tb_patchify
+    assert split(16, 9, 5, shape, 4, 8, 3, 0, ptrs, None) == tbl.TB_ERR_DTYPE
+    assert split(16, 2, 0, shape, 0, 8, 3, 0, ptrs, None) == tbl.TB_ERR_SHAPE       # ndim
+    assert split(16, 2, 9, shape, 0, 8, 3, 0, ptrs, None) == tbl.TB_ERR_SHAPE       # ndim
+    assert split(16, 2, 5, shape, 5, 8, 3, 0, ptrs, None) == tbl.TB_ERR_SHAPE       # axis
+    assert split(16, 2, 5, shape, 4, 24, 3, 0, ptrs, None) == tbl.TB_ERR_SHAPE      # 208 is not whole bands of 24
+    assert split(16, 2, 5, shape, 4, 8, 3, 71, ptrs, None) == tbl.TB_ERR_SHAPE      # slot < the largest band (72)
+    assert split(16, 2, 5, shape, 4, 8, 3, -1, ptrs, None) == tbl.TB_ERR_SHAPE
+    assert split(16, 2, 5, shape, 4, 8, 65, 0, ptrs, None) == tbl.TB_ERR_UNSUPPORTED
+    assert split(None, 2, 5, shape, 4, 8, 3, 0, ptrs, None) == tbl.TB_ERR_NULL
+    assert split(16, 2, 5, None, 4, 8, 3, 0, ptrs, None) == tbl.TB_ERR_NULL
+    assert split(16, 2, 5, shape, 4, 8, 3, 0, None, None) == tbl.TB_ERR_NULL
+    assert split(16, 2, 5, shape, 4, 8, 3, 0, (ctypes.c_void_p * 3)(16, None, 48), None) == tbl.TB_ERR_NULL
+    neg = (ctypes.c_int64 * 5)(1, -384, 13, 120, 208)
+    assert split(16, 2, 5, neg, 4, 8, 3, 0, ptrs, None) == tbl.TB_ERR_SHAPE
+    # nothing to move: success without a launch, whatever the pointers
+    empty = (ctypes.c_int64 * 5)(0, 384, 13, 120, 208)
+    assert split(None, 2, 5, empty, 4, 8, 3, 0, (ctypes.c_void_p * 3)(), None) == tbl.TB_OK
+    # more ranks than bands: the empty patches need no pointer (still no launch here)
+    small = (ctypes.c_int64 * 2)(0, 16)
+    assert split(None, 2, 2, small, 1, 8, 4, 0, (ctypes.c_void_p * 4)(), None) == tbl.TB_OK
+
+    gather = tbl._lib.tb_gather_patches
+    sizes = (ctypes.c_int64 * 3)(72, 72, 64)
+    assert gather(ptrs, 3, (ctypes.c_int64 * 3)(72, 72, 63), 2, 5, shape, 4, 0, 16, None) == tbl.TB_ERR_SHAPE
+    assert gather(ptrs, 3, (ctypes.c_int64 * 3)(72, -8, 144), 2, 5, shape, 4, 0, 16, None) == tbl.TB_ERR_SHAPE
+    assert gather(ptrs, 3, None, 2, 5, shape, 4, 0, 16, None) == tbl.TB_ERR_NULL
+    assert gather(ptrs, 0, sizes, 2, 5, shape, 4, 0, 16, None) == tbl.TB_ERR_SHAPE
+    assert gather(ptrs, 3, sizes, 2, 5, shape, 4, 0, None, None) == tbl.TB_ERR_NULL
+    assert gather(ptrs, 3, sizes, 2, 5, shape, 4, 70, 16, None) == tbl.TB_ERR_SHAPE
+    assert gather(ptrs, 3, sizes, 7, 5, shape, 4, 0, 16, None) == tbl.TB_ERR_DTYPE
+    # any sizes, not only whole bands, as long as they sum to the axis
+    odd = (ctypes.c_int64 * 3)(1, 0, 207)
+    assert gather((ctypes.c_void_p * 3)(16, None, 48), 3, odd, 2, 5, empty, 4, 0, 16, None) == tbl.TB_OK
