@@ -32,6 +32,14 @@
 #ifndef TB_STITCH_ROWS_PER_THREAD_3D
 #define TB_STITCH_ROWS_PER_THREAD_3D 64
 #endif
+// Ramp stitch pieces: rows per thread start at the maximum and halve while
+// the grid has fewer than this many pieces per SM.
+#ifndef TB_RAMP_PIECES_PER_SM
+#define TB_RAMP_PIECES_PER_SM 3
+#endif
+#ifndef TB_RAMP_MAX_ROWS_PER_THREAD
+#define TB_RAMP_MAX_ROWS_PER_THREAD 16
+#endif
 // Cluster size of the GroupNorm statistics kernel; 0 picks it from occupancy.
 #ifndef TB_GN_FORCE_CS
 #define TB_GN_FORCE_CS 0
@@ -577,18 +585,37 @@ TB_API tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int6
     for (int64_t q = 0; q < ntiles; ++q) prm.tiles[q] = tiles[q];
     prm.out = out;
     prm.planes = planes;
-    int max_pieces = 1;
-    for (int sx = 0; sx < prm.ax.nseg; ++sx) {
-        const int width = prm.ax.seg_len[sx] / vec;
-        const int bdx = std::max(1, std::min(width, tb::ramp_block()));
-        const int bdy = tb::ramp_block() / bdx;
-        prm.rows_per_piece[sx] = bdy * 16;
-        for (int sy = 0; sy < prm.ay.nseg; ++sy)
-            max_pieces = std::max(max_pieces, (prm.ay.seg_len[sy] + prm.rows_per_piece[sx] - 1) / prm.rows_per_piece[sx]);
+    // A piece is a run of rows of one rectangle with every plane's rows laid
+    // end to end, so rectangles a few rows high still fill whole CTAs.  Rows
+    // per thread start at TB_RAMP_MAX_ROWS_PER_THREAD and halve (down to 2)
+    // while there are fewer than TB_RAMP_PIECES_PER_SM pieces per SM.  The
+    // grid is (rectangle, piece index).
+    if (planes * ay->out_extent > 2147483647LL - 4LL * tb::ramp_block()) return TB_ERR_UNSUPPORTED;
+    int sms = 0;
+    st = device_sms(&sms);
+    if (st != TB_OK) return st;
+    int64_t max_pieces = 1;
+    for (int rpt = TB_RAMP_MAX_ROWS_PER_THREAD;; rpt /= 2) {
+        for (int sx = 0; sx < prm.ax.nseg; ++sx) {
+            const int width = prm.ax.seg_len[sx] / vec;
+            const int bdx = std::max(1, std::min(width, tb::ramp_block()));
+            prm.rows_per_piece[sx] = (tb::ramp_block() / bdx) * rpt;
+        }
+        int64_t total = 0;
+        max_pieces = 1;
+        for (int sy = 0; sy < prm.ay.nseg; ++sy) {
+            const int64_t flat = planes * prm.ay.seg_len[sy];
+            for (int sx = 0; sx < prm.ax.nseg; ++sx) {
+                const int64_t n = (flat + prm.rows_per_piece[sx] - 1) / prm.rows_per_piece[sx];
+                total += n;
+                max_pieces = std::max(max_pieces, n);
+            }
+        }
+        if (total >= (int64_t)TB_RAMP_PIECES_PER_SM * sms || rpt <= 2) break;
     }
-    const int64_t gx = planes * prm.ay.nseg * prm.ax.nseg;
-    if (gx > 2147483647LL || max_pieces > 65535) return TB_ERR_UNSUPPORTED;
-    cudaError_t e = tb::launch_ramp(prm, (int)dtype, vec, (int)gx, max_pieces, reinterpret_cast<cudaStream_t>(stream));
+    if (max_pieces > 65535) return TB_ERR_UNSUPPORTED;
+    cudaError_t e = tb::launch_ramp(prm, (int)dtype, vec, prm.ay.nseg * prm.ax.nseg, (int)max_pieces,
+                                    reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return TB_OK;
 }

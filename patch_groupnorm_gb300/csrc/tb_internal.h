@@ -146,7 +146,7 @@ struct RampParams {
     void* out;
     int64_t planes;
     RampAxisK ay, ax;
-    int32_t rows_per_piece[RAMP_MAXSEG];  // by width segment
+    int32_t rows_per_piece[RAMP_MAXSEG];  // flattened (plane, row) rows per piece, by width segment
 };
 static_assert(sizeof(RampParams) <= 32000, "kernel parameter block too large");
 

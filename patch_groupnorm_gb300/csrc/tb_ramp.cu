@@ -14,10 +14,12 @@
 // which the set of tiles with positive weight is constant (at 16-byte chunk
 // granularity along the width); the canvas then splits into rectangles with
 // a fixed number of source tiles.  A CTA takes a run of rows of one
-// rectangle for one (batch, channel) plane and runs a path compiled for its
-// (height cover, width cover) in {1, 2, 3}^2; a rectangle covered by one tile
-// is an exact copy (w / w = 1).  Loads stream through a per-thread cp.async
-// ring in shared memory, as in the recurrence stitch.
+// rectangle, the rows of all (batch, channel) planes laid end to end so that
+// rectangles only a few rows high (latent-space tiles) still fill a CTA, and
+// runs a path compiled for its (height cover, width cover) in {1, 2, 3}^2; a
+// rectangle covered by one tile is an exact copy (w / w = 1).  Loads stream
+// through a per-thread cp.async ring in shared memory, as in the recurrence
+// stitch.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -134,9 +136,22 @@ __device__ __forceinline__ float axis_w(const RampAxisK& A, int seg, int a, int 
     return ramp_weight(pos - A.org[t], A.T, t > 0, t < A.n - 1, A.zero, A.inv_ramp);
 }
 
+// Position of a row in the flattened (plane, row) space of one rectangle,
+// stepped `bdy` rows at a time without division.
+struct FlatRow {
+    int plane, yl;
+    __device__ __forceinline__ void advance(int sq, int sr, int len) {
+        plane += sq;
+        yl += sr;
+        if (yl >= len) {
+            yl -= len;
+            ++plane;
+        }
+    }
+};
+
 template <int CY, int CX, int DT, int VEC>
-__device__ __forceinline__ void run_rect(const RampParams& p, int64_t plane, int sy, int sx, int rbeg, int rend,
-                                         uint32_t s_ring) {
+__device__ __forceinline__ void run_rect(const RampParams& p, int sy, int sx, int fbeg, int fend, uint32_t s_ring) {
     constexpr int NU = CY * CX;
     constexpr int S = RAMP_SLOTS / NU >= 2 ? RAMP_SLOTS / NU : 1;
     const RampAxisK& AY = p.ay;
@@ -167,26 +182,30 @@ __device__ __forceinline__ void run_rect(const RampParams& p, int64_t plane, int
                 for (int b = 0; b < CX; ++b) wx[b][l] *= inv;
             }
         }
-        // sources: tile (Y.tile[a], X.tile[b]) at row 0 of the canvas
+        // sources: tile (Y.tile[a], X.tile[b]) at plane 0, canvas row y0
+        const int y0 = AY.seg_start[sy];
         const char* src[NU];
-        int32_t pitch[CX];
-#pragma unroll
-        for (int b = 0; b < CX; ++b) pitch[b] = AX.T * RElt<DT>::BYTES;
+        const int32_t pitch = AX.T * RElt<DT>::BYTES;
+        const int64_t tplane = (int64_t)AY.T * AX.T * RElt<DT>::BYTES;
 #pragma unroll
         for (int a = 0; a < CY; ++a)
 #pragma unroll
             for (int b = 0; b < CX; ++b) {
                 const int ti = AY.seg_tile[sy][a], tj = AX.seg_tile[sx][b];
-                // element (plane, y - oy, x0 - ox) of tile (ti, tj) is src + y * pitch
+                // element (plane, y0 + yl - oy, x0 - ox) of tile (ti, tj) is
+                // src + plane * tplane + yl * pitch
                 src[a * CX + b] = reinterpret_cast<const char*>(p.tiles[ti * AX.n + tj]) +
-                                  (((plane * AY.T) - AY.org[ti]) * (int64_t)AX.T + (x0 - AX.org[tj])) *
-                                      RElt<DT>::BYTES;
+                                  ((int64_t)(y0 - AY.org[ti]) * AX.T + (x0 - AX.org[tj])) * RElt<DT>::BYTES;
             }
-        char* dst = reinterpret_cast<char*>(p.out) + ((plane * AY.out) * (int64_t)AX.out + x0) * RElt<DT>::BYTES;
+        char* dst = reinterpret_cast<char*>(p.out) + ((int64_t)y0 * AX.out + x0) * RElt<DT>::BYTES;
         const int32_t opitch = AX.out * RElt<DT>::BYTES;
+        const int64_t oplane = (int64_t)AY.out * AX.out * RElt<DT>::BYTES;
 
-        const int r0 = rbeg + ty;
-        const int nrows = r0 < rend ? (rend - r0 + bdy - 1) / bdy : 0;
+        const int len = AY.seg_len[sy];
+        const int sq = bdy / len, sr = bdy % len;
+        const int r0 = fbeg + ty;
+        const int nrows = r0 < fend ? (fend - r0 + bdy - 1) / bdy : 0;
+        const FlatRow first = {r0 / len, r0 % len};
         // combine the CY x CX source values of one row; x_ab(l) reads them
         auto combine = [&](int y, auto x_ab) {
             float wy[CY];
@@ -221,48 +240,53 @@ __device__ __forceinline__ void run_rect(const RampParams& p, int64_t plane, int
             return acc_pack<DT, VEC>(acc);
         };
         if constexpr (VEC * RElt<DT>::BYTES == 16) {
+            FlatRow ahead = first;  // the next row to issue
             auto issue = [&](int m) {
-                const int y = AY.seg_start[sy] + r0 + m * bdy;
+                const int64_t off = ahead.plane * tplane + (int64_t)ahead.yl * pitch;
                 const uint32_t st = my_slot + (uint32_t)((m % S) * NU) * slot_stride;
 #pragma unroll
-                for (int n = 0; n < NU; ++n)
-                    cp_async16(st + (uint32_t)n * slot_stride, src[n] + (int64_t)y * pitch[n % CX]);
+                for (int n = 0; n < NU; ++n) cp_async16(st + (uint32_t)n * slot_stride, src[n] + off);
+                ahead.advance(sq, sr, len);
             };
 #pragma unroll
             for (int m = 0; m < S - 1; ++m) {
                 if (m < nrows) issue(m);
                 cp_async_commit();
             }
+            FlatRow at = first;
             for (int m = 0; m < nrows; ++m) {
                 if (m + S - 1 < nrows) issue(m + S - 1);
                 cp_async_commit();
                 cp_async_wait<S - 1>();
-                const int y = AY.seg_start[sy] + r0 + m * bdy;
                 const uint32_t st = my_slot + (uint32_t)((m % S) * NU) * slot_stride;
                 uint4 o;
                 if constexpr (NU == 1) {
                     o = lds16(st);  // one tile: its normalised weight is exactly 1
                 } else {
-                    o = combine(y, [&](int a, int b, float (&x)[VEC]) {
+                    o = combine(y0 + at.yl, [&](int a, int b, float (&x)[VEC]) {
                         const uint4 v = lds16(st + (uint32_t)(a * CX + b) * slot_stride);
                         unpack_chunk<DT, VEC>(v, x);
                     });
                 }
-                __stcs(reinterpret_cast<uint4*>(dst + (int64_t)y * opitch), o);
+                __stcs(reinterpret_cast<uint4*>(dst + at.plane * oplane + (int64_t)at.yl * opitch), o);
+                at.advance(sq, sr, len);
             }
             cp_async_wait<0>();
         } else {
             // element path (unaligned geometry): plain loads, one row at a time
+            FlatRow at = first;
             for (int m = 0; m < nrows; ++m) {
-                const int y = AY.seg_start[sy] + r0 + m * bdy;
+                const int64_t off = at.plane * tplane + (int64_t)at.yl * pitch;
+                char* const o_at = dst + at.plane * oplane + (int64_t)at.yl * opitch;
                 if constexpr (NU == 1) {
-                    store_elem<DT>(dst + (int64_t)y * opitch, load_elem<DT>(src[0] + (int64_t)y * pitch[0]));
+                    store_elem<DT>(o_at, load_elem<DT>(src[0] + off));
                 } else {
-                    const uint4 o = combine(y, [&](int a, int b, float (&x)[VEC]) {
-                        x[0] = elem_value<DT>(load_elem<DT>(src[a * CX + b] + (int64_t)y * pitch[b]));
+                    const uint4 o = combine(y0 + at.yl, [&](int a, int b, float (&x)[VEC]) {
+                        x[0] = elem_value<DT>(load_elem<DT>(src[a * CX + b] + off));
                     });
-                    store_elem<DT>(dst + (int64_t)y * opitch, o.x);
+                    store_elem<DT>(o_at, o.x);
                 }
+                at.advance(sq, sr, len);
             }
         }
     }
@@ -271,29 +295,31 @@ __device__ __forceinline__ void run_rect(const RampParams& p, int64_t plane, int
 template <int DT, int VEC>
 __global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_constant__ RampParams p) {
     extern __shared__ __align__(16) unsigned char s_ring[];
-    // blockIdx.x: (plane, rectangle) with the rectangle fastest; blockIdx.y:
-    // run of rows inside the rectangle
-    const int nrect = p.ay.nseg * p.ax.nseg;
-    const int rect = (int)(blockIdx.x % (unsigned)nrect);
-    const int64_t plane = blockIdx.x / (unsigned)nrect;
-    const int sy = rect / p.ax.nseg, sx = rect % p.ax.nseg;
-    const int rows = p.ay.seg_len[sy];
-    const int rbeg = blockIdx.y * p.rows_per_piece[sx];
-    if (rbeg >= rows) return;
-    const int rend = min(rows, rbeg + p.rows_per_piece[sx]);
+    // A piece is a run of rows of one rectangle, in the rectangle's (plane,
+    // row) space flattened over all planes.  blockIdx.x is the rectangle
+    // (row-major over (sy, sx)) and blockIdx.y the piece index, so the CTAs
+    // launched first cover every rectangle, i.e. whole rows of the canvas;
+    // rectangles with fewer pieces leave their trailing CTAs empty.
+    const int sy = (int)blockIdx.x / p.ax.nseg;
+    const int sx = (int)blockIdx.x % p.ax.nseg;
+    const int rem = (int)blockIdx.y;
+    const int flat = (int)p.planes * p.ay.seg_len[sy];
+    const int fbeg = rem * p.rows_per_piece[sx];
+    if (fbeg >= flat) return;
+    const int fend = min(flat, fbeg + p.rows_per_piece[sx]);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(s_ring);
     const int cy = p.ay.seg_n[sy], cx = p.ax.seg_n[sx];
     switch (cy * 4 + cx) {
-        case 5: run_rect<1, 1, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
-        case 6: run_rect<1, 2, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
-        case 7: run_rect<1, 3, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
-        case 9: run_rect<2, 1, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
-        case 10: run_rect<2, 2, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
-        case 11: run_rect<2, 3, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
-        case 13: run_rect<3, 1, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
-        case 14: run_rect<3, 2, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
-        case 15: run_rect<3, 3, DT, VEC>(p, plane, sy, sx, rbeg, rend, ring); break;
+        case 5: run_rect<1, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+        case 6: run_rect<1, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+        case 7: run_rect<1, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+        case 9: run_rect<2, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+        case 10: run_rect<2, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+        case 11: run_rect<2, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+        case 13: run_rect<3, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+        case 14: run_rect<3, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+        case 15: run_rect<3, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
         default: break;
     }
 }
