@@ -19,12 +19,17 @@
 //     mean = meanA + d * nB / n,  M2 = M2A + M2B + d^2 * nA * nB / n.
 //
 // gn_stats_kernel: one thread-block cluster per (patch, sample, group), sized
-// to about two CTAs per SM in all.  Each thread keeps eight 128-bit streaming
-// loads in flight and folds each batch (64 bf16 / fp16 or 32 fp32 elements)
-// into its running triple with Chan's update after computing the batch's own
-// mean and M2 directly; warps merge with shuffles, warps within a CTA through
-// shared memory, and the CTAs of the cluster through distributed shared
-// memory, in a fixed order (deterministic results).
+// to about two CTAs per SM in all.  Each thread streams 16-byte chunks through
+// a ring of cp.async slots, seven ahead.  For fp16 / bf16 it sums x - K and
+// (x - K)^2 over groups of 8 chunks (64 elements) on packed fp32 pairs, K
+// being the group's first element -- differences and squares of 16-bit
+// values are nearly always exact in fp32, and the shift keeps
+// M2 = S2 - S1^2 / m from cancelling -- and folds each group into its
+// running triple with Chan's update; fp32 chunks are folded one by one after
+// their own mean and M2 are computed directly.  Warps merge with shuffles,
+// warps within a CTA through shared memory, and the CTAs of the cluster
+// through distributed shared memory, in a fixed order (deterministic
+// results).
 //
 // Both kernels are launched with programmatic stream serialisation: their
 // parameter-only prologue may overlap the preceding kernel, and they execute
@@ -53,6 +58,10 @@ namespace {
 #endif
 constexpr int STATS_BLOCK = TB_GN_STATS_BLOCK;
 constexpr int STATS_SLOTS = TB_GN_STATS_SLOTS;  // cp.async ring slots per thread (16 bytes each)
+#ifndef TB_GN_STATS_GROUP
+#define TB_GN_STATS_GROUP 8
+#endif
+constexpr int STATS_GROUP = TB_GN_STATS_GROUP;  // 16-bit chunks per shifted-sum group
 constexpr int APPLY_BLOCK = 128;
 constexpr int APPLY_CPT = 4;  // 16-byte chunks per thread per segment
 
@@ -173,6 +182,48 @@ __device__ __forceinline__ Stat chan_fast(const Stat& a, const Stat& b) {
     return s;
 }
 
+// Shifted sums of the two 16-bit lanes of word v, on packed fp32 pairs:
+// s1 += x - K, s2 += (x - K)^2 (k2 holds K in both lanes).
+template <int DT>
+__device__ __forceinline__ void shifted_acc(uint32_t v, unsigned long long k2, unsigned long long& s1,
+                                            unsigned long long& s2) {
+    if constexpr (DT == BF16) {
+        asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 x, d;\n\t"
+            "shl.b32 lo, %2, 16;\n\t"
+            "and.b32 hi, %2, 0xffff0000;\n\t"
+            "mov.b64 x, {lo, hi};\n\t"
+            "sub.rn.f32x2 d, x, %3;\n\t"
+            "add.rn.f32x2 %0, %0, d;\n\t"
+            "fma.rn.f32x2 %1, d, d, %1;\n\t}"
+            : "+l"(s1), "+l"(s2)
+            : "r"(v), "l"(k2));
+    } else {
+        asm("{\n\t.reg .b16 hl, hh;\n\t.reg .b32 lo, hi;\n\t.reg .b64 x, d;\n\t"
+            "mov.b32 {hl, hh}, %2;\n\t"
+            "cvt.f32.f16 lo, hl;\n\t"
+            "cvt.f32.f16 hi, hh;\n\t"
+            "mov.b64 x, {lo, hi};\n\t"
+            "sub.rn.f32x2 d, x, %3;\n\t"
+            "add.rn.f32x2 %0, %0, d;\n\t"
+            "fma.rn.f32x2 %1, d, d, %1;\n\t}"
+            : "+l"(s1), "+l"(s2)
+            : "r"(v), "l"(k2));
+    }
+}
+
+__device__ __forceinline__ float lane_sum(unsigned long long v) {
+    return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
+}
+
+// (count, mean, M2) of a group of m elements from its shifted sums about K:
+// mean = K + s1 / m, M2 = s2 - s1^2 / m.  K is the group's first element,
+// so the shift removes the group's offset and the subtraction loses little.
+__device__ __forceinline__ Stat shifted_stat(unsigned long long s1, unsigned long long s2, float K, float m) {
+    const float a = lane_sum(s1), b = lane_sum(s2);
+    const float q = __fdividef(a, m);
+    return Stat{m, K + q, fmaxf(0.f, fmaf(-a, q, b))};
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gptr) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(saddr), "l"(gptr) : "memory");
 }
@@ -229,15 +280,44 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
             if (k < cnt) cp_async16(ring + k * SLOT, src + first + (int64_t)k * STATS_BLOCK);
             cp_async_commit();
         }
-        for (int k = 0; k < cnt; ++k) {
-            const int ahead = k + STATS_SLOTS - 1;
-            if (ahead < cnt)
-                cp_async16(ring + (ahead % STATS_SLOTS) * SLOT, src + first + (int64_t)ahead * STATS_BLOCK);
-            cp_async_commit();
-            cp_async_wait<STATS_SLOTS - 1>();
-            float x[VEC];
-            chunk_to_floats<DT>(lds16(ring + (k % STATS_SLOTS) * SLOT), x);
-            acc = k == 0 ? block_stat<VEC>(x) : chan_fast(acc, block_stat<VEC>(x));
+        if constexpr (GElt<DT>::BYTES == 2) {
+            // Groups of STATS_GROUP chunks: shifted sums about the group's
+            // first element on packed fp32 pairs (3 packed operations per
+            // element pair), then one Chan merge per group.
+            unsigned long long s1 = 0, s2 = 0, k2 = 0;
+            float K = 0.f;
+            for (int k = 0; k < cnt; ++k) {
+                const int ahead = k + STATS_SLOTS - 1;
+                if (ahead < cnt)
+                    cp_async16(ring + (ahead % STATS_SLOTS) * SLOT, src + first + (int64_t)ahead * STATS_BLOCK);
+                cp_async_commit();
+                cp_async_wait<STATS_SLOTS - 1>();
+                const uint4 v = lds16(ring + (k % STATS_SLOTS) * SLOT);
+                if ((k % STATS_GROUP) == 0) {
+                    if (k > 0) acc = chan_fast(acc, shifted_stat(s1, s2, K, (float)(STATS_GROUP * VEC)));
+                    K = GElt<DT>::to_f(v.x);
+                    const unsigned long long kb = __float_as_uint(K);
+                    k2 = kb | (kb << 32);
+                    s1 = 0;
+                    s2 = 0;
+                }
+                shifted_acc<DT>(v.x, k2, s1, s2);
+                shifted_acc<DT>(v.y, k2, s1, s2);
+                shifted_acc<DT>(v.z, k2, s1, s2);
+                shifted_acc<DT>(v.w, k2, s1, s2);
+            }
+            if (cnt > 0) acc = chan_fast(acc, shifted_stat(s1, s2, K, (float)(((cnt - 1) % STATS_GROUP + 1) * VEC)));
+        } else {
+            for (int k = 0; k < cnt; ++k) {
+                const int ahead = k + STATS_SLOTS - 1;
+                if (ahead < cnt)
+                    cp_async16(ring + (ahead % STATS_SLOTS) * SLOT, src + first + (int64_t)ahead * STATS_BLOCK);
+                cp_async_commit();
+                cp_async_wait<STATS_SLOTS - 1>();
+                float x[VEC];
+                chunk_to_floats<DT>(lds16(ring + (k % STATS_SLOTS) * SLOT), x);
+                acc = k == 0 ? block_stat<VEC>(x) : chan_fast(acc, block_stat<VEC>(x));
+            }
         }
         cp_async_wait<0>();
     } else {
@@ -417,7 +497,7 @@ size_t stats_smem(bool aligned) { return aligned ? (size_t)STATS_SLOTS * STATS_B
 template <int DT>
 cudaError_t stats_dt(const GnStatsParams& p, int64_t units, cudaStream_t s) {
     void (*fn)(const GnStatsParams) = stats_fn<DT>(p.aligned != 0);
-    if (stats_smem(p.aligned != 0) > 48 * 1024) {
+    if (stats_smem(p.aligned != 0) > 40 * 1024) {  // with the static shared memory, past the 48 KB default
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)stats_smem(p.aligned != 0));
         if (e != cudaSuccess) return e;

@@ -69,6 +69,30 @@ __host__ __device__ inline BoxShape box_shape(int b, int Kt, int Ky, int Kx, int
     return s;
 }
 
+#ifdef __CUDACC__
+// Every kernel is launched with programmatic stream serialisation and runs
+// griddepcontrol.wait before its first global-memory access.  Triggering at
+// the start of each CTA lets the next kernel in the stream launch as soon as
+// every CTA of this grid has started (so it never takes a slot this grid
+// still needs); its CTAs run their parameter-only prologue and then wait for
+// this grid to complete and its writes to become visible.  Only the stitch
+// triggers: its grids run many waves, and the next grid fills the SMs as the
+// last wave drains (small stitches 12-18% faster back to back).  The
+// GroupNorm statistics grid is one wave spread evenly over the SMs, and a
+// grid placed early, while its predecessor drains, lands unevenly (measured
+// up to 2x slower); so no kernel that may precede it in a sharded decode --
+// the Patchify copy, the GroupNorm kernels themselves -- triggers, and the
+// ramp stitch measured no gain from it.
+#ifndef TB_PDL_TRIGGER
+#define TB_PDL_TRIGGER 1
+#endif
+__device__ __forceinline__ void pdl_trigger_dependents() {
+#if TB_PDL_TRIGGER
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+#endif
+
 // Thread layout of a CTA on a box `width` chunks wide: bdx threads across,
 // bdy rows at a time, each thread covering cpt columns.
 __host__ __device__ inline void box_layout(int width, int& bdx, int& bdy, int& cpt) {

@@ -579,6 +579,7 @@ __device__ __forceinline__ void run_box_pipe(const StitchParams<MAXA, MAXT, MAXC
 template <int NDIM, int DT, int VEC, int MAXA, int MAXT, int MAXC>
 __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_3D : TB_STITCH_MIN_CTAS_2D))
     stitch_kernel(const __grid_constant__ StitchParams<MAXA, MAXT, MAXC> p) {
+    pdl_trigger_dependents();
     extern __shared__ __align__(16) unsigned char s_dyn[];
     const auto& AT = p.ax[0];
     const auto& AY = p.ax[1];
