@@ -1,0 +1,92 @@
+"""CUDA-graph replay of the sharded-decode steps (Patchify split, PatchGroupNorm
+statistics and normalisation, patch gather) and of the ramp stitch, captured
+once and replayed with new contents at the same addresses.  Every call passes
+its parameters by value, so each replay must reproduce the oracle's result
+for the inputs present at replay time."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import groupnorm as GN
+from oracle import rounding as R
+from oracle.ramp import ramp_stitch_2d
+from patch_groupnorm_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tbl():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from patch_groupnorm_gb300 import build
+    build.build()
+    from patch_groupnorm_gb300 import tileblend
+    return tileblend
+
+
+def _within_one_ulp(got: torch.Tensor, exact: np.ndarray, dtype: str) -> bool:
+    ref = R.storage_to_f64(R.round_f64(exact, dtype), dtype)
+    mant = 10 if dtype == "f16" else 7
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -8))) - mant)
+    return bool((np.abs(got.double().cpu().numpy() - ref) <= ulp).all())
+
+
+def test_sharded_groupnorm_pipeline_replays_with_new_inputs(tbl):
+    shape, axis, factor, ranks, G = (1, 64, 15, 24), 2, 1, 2, 8
+    x = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    x.copy_(synth.normal_tensor(1, shape, "bf16"))
+    gamma = synth.normal_tensor(2, (64,), "bf16").cuda() * 0.1 + 1.0
+    beta = synth.normal_tensor(3, (64,), "bf16").cuda() * 0.1
+    _, sizes = tbl.tb_patchify_layout(shape[axis], factor, ranks)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):   # allocate and warm up outside the capture
+        parts = tbl.tb_patchify(x, axis, factor, ranks)
+        outs = [torch.empty_like(p) for p in parts]
+        partials = tbl.new_partials(ranks, 1, G)
+        whole = torch.empty_like(x)
+        tbl.tb_patch_gn_stats(parts, G, partials)
+        tbl.tb_patch_gn_apply(parts, outs, G, partials, gamma, beta, 1e-6, True)
+        tbl.tb_gather_patches(outs, sizes, axis, out=whole)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tbl.tb_patchify(x, axis, factor, ranks, patches=parts)
+        tbl.tb_patch_gn_stats(parts, G, partials)
+        tbl.tb_patch_gn_apply(parts, outs, G, partials, gamma, beta, 1e-6, True)
+        tbl.tb_gather_patches(outs, sizes, axis, out=whole)
+    for seed in (21, 22, 23):
+        fresh = synth.normal_tensor(seed, shape, "bf16") * (1.0 + seed % 3) + (seed - 22)
+        x.copy_(fresh.to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        exact = GN.patch_group_norm([x.double().cpu().numpy()], G, gamma.double().cpu().numpy(),
+                                    beta.double().cpu().numpy(), 1e-6, silu=True)[0]
+        assert _within_one_ulp(whole, exact, "bf16"), seed
+
+
+def test_ramp_stitch_replays_with_new_inputs(tbl):
+    ay = tbl.RampAxis.spread(64, 32, 3, 8)
+    ax = tbl.RampAxis.spread(96, 32, 5, 8)
+    shape = (1, 2, ay.tile_extent, ax.tile_extent)
+    tiles = [[torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in ax.origins] for _ in ay.origins]
+    out = torch.empty((1, 2, ay.out_extent, ax.out_extent), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        tbl.tb_stitch2d_ramp(tiles, ay, ax, out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tbl.tb_stitch2d_ramp(tiles, ay, ax, out)
+    rng = np.random.default_rng(5)
+    for _ in range(3):
+        host = [[torch.from_numpy(rng.uniform(-1, 1, shape)).to(torch.bfloat16) for _ in ax.origins]
+                for _ in ay.origins]
+        for rd, rh in zip(tiles, host):
+            for td, th in zip(rd, rh):
+                td.copy_(th)
+        g.replay()
+        torch.cuda.synchronize()
+        exact = ramp_stitch_2d([[t.double().numpy() for t in row] for row in host], ay.origins, ax.origins,
+                               ay.tile_extent, ax.tile_extent, (ay.out_extent, ax.out_extent), ay.zero, ay.ramp,
+                               ax.zero, ax.ramp)
+        assert _within_one_ulp(out, exact, "bf16")
