@@ -96,3 +96,65 @@ def test_small_layouts(tbl, dtype, layout):
     tiles = [[torch.from_numpy(rng.uniform(-1, 1, (2, 3, ay.tile_extent, ax.tile_extent))).to(TORCH[dtype])
               for _ in ax.origins] for _ in ay.origins]
     _check(tbl, tiles, ay, ax, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_one_tile_and_one_row_of_tiles(tbl, dtype):
+    rng = np.random.default_rng(30)
+    # a single tile is the canvas: copied exactly
+    a1 = tbl.RampAxis.spread(32, 32, 1, 8)
+    t = torch.from_numpy(rng.uniform(-1, 1, (2, 3, 256, 256))).to(TORCH[dtype])
+    got = _run(tbl, [[t]], a1, a1, dtype)
+    assert np.array_equal(to_storage(got, dtype), to_storage(t, dtype))
+    # one row of tiles along the width: blends along x only
+    ax = tbl.RampAxis.spread(96, 32, 4, 8)
+    tiles = [[torch.from_numpy(rng.uniform(-1, 1, (1, 2, 256, ax.tile_extent))).to(TORCH[dtype])
+              for _ in ax.origins]]
+    _check(tbl, tiles, a1, ax, dtype)
+
+
+def test_misaligned_pointers_take_the_element_path(tbl):
+    ay = tbl.RampAxis.spread(64, 32, 3, 8)
+    ax = tbl.RampAxis.spread(96, 32, 5, 8)
+    rng = np.random.default_rng(31)
+    shape = (1, 2, ay.tile_extent, ax.tile_extent)
+    host = [[torch.from_numpy(rng.uniform(-1, 1, shape)).to(torch.bfloat16) for _ in ax.origins] for _ in ay.origins]
+    keep, dev = [], []
+    for row in host:
+        drow = []
+        for t in row:
+            buf = torch.empty(t.numel() + 1, dtype=torch.bfloat16, device="cuda")
+            v = buf[1:].view(shape)     # 2 bytes past a 16-byte boundary
+            v.copy_(t)
+            keep.append(buf)
+            drow.append(v)
+        dev.append(drow)
+    out = torch.empty((1, 2, ay.out_extent, ax.out_extent), dtype=torch.bfloat16, device="cuda")
+    tbl.tb_stitch2d_ramp(dev, ay, ax, out)
+    torch.cuda.synchronize()
+    exact = ramp_stitch_2d([[t.double().numpy() for t in row] for row in host], ay.origins, ax.origins,
+                           ay.tile_extent, ax.tile_extent, (ay.out_extent, ax.out_extent), ay.zero, ay.ramp,
+                           ax.zero, ax.ramp)
+    ref = R.storage_to_f64(R.round_f64(exact, "bf16"), "bf16")
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -8))) - 7)
+    assert (np.abs(out.double().cpu().numpy() - ref) <= ulp).all()
+
+
+def test_empty_batch_and_guard_bands(tbl):
+    ay = tbl.RampAxis.spread(64, 32, 3, 8)
+    ax = tbl.RampAxis.spread(96, 32, 5, 8)
+    empty = [[torch.empty((0, 3, ay.tile_extent, ax.tile_extent), device="cuda") for _ in ax.origins]
+             for _ in ay.origins]
+    tbl.tb_stitch2d_ramp(empty, ay, ax, torch.empty((0, 3, ay.out_extent, ax.out_extent), device="cuda"))
+    # the output between two canary bands: nothing outside it is written
+    rng = np.random.default_rng(32)
+    tiles = [[torch.from_numpy(rng.uniform(-1, 1, (1, 3, ay.tile_extent, ax.tile_extent))).float().cuda()
+              for _ in ax.origins] for _ in ay.origins]
+    n = 3 * ay.out_extent * ax.out_extent
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 777.0, device="cuda")
+    out = buf[guard:guard + n].view(1, 3, ay.out_extent, ax.out_extent)
+    tbl.tb_stitch2d_ramp(tiles, ay, ax, out)
+    torch.cuda.synchronize()
+    assert (buf[:guard] == 777.0).all() and (buf[guard + n:] == 777.0).all()
+    assert torch.isfinite(out).all()

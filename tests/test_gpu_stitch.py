@@ -260,3 +260,24 @@ def test_graph_capture_replays_with_new_inputs(tbl):
         torch.cuda.synchronize()
         ref = oracle_stitch(_storage_grid(fresh, "f32"), lays, "f32")
         _check_equal(out.cpu(), ref, "f32")
+
+
+@pytest.mark.parametrize("ndim", [2, 3])
+def test_largest_tile_grid_bit_exact(tbl, ndim):
+    # TB_MAX_TILES tiles in one call: 16 x 64 (2D) and 4 x 16 x 16 (3D) small
+    # tiles, 64 along one axis (TB_MAX_TILES_PER_AXIS)
+    if ndim == 2:
+        axes = [W.AxisSpec(96, 8, 0.25, 1), W.AxisSpec(384, 8, 0.25, 1)]
+    else:
+        axes = [W.AxisSpec(24, 8, 0.25, 1), W.AxisSpec(96, 8, 0.25, 1), W.AxisSpec(96, 8, 0.25, 1)]
+    lays = _oracle_layouts(axes)
+    assert int(np.prod([l.n for l in lays])) == tbl.TB_MAX_TILES
+    rng = np.random.default_rng(40 + ndim)
+    if ndim == 2:
+        tiles = [[torch.from_numpy(rng.uniform(-1, 1, (1, 2, ly, lx))).to(torch.bfloat16)
+                  for lx in lays[1].extents] for ly in lays[0].extents]
+    else:
+        tiles = [[[torch.from_numpy(rng.uniform(-1, 1, (1, 2, lt, ly, lx))).to(torch.bfloat16)
+                   for lx in lays[2].extents] for ly in lays[1].extents] for lt in lays[0].extents]
+    ref = oracle_stitch(_storage_grid(tiles, "bf16"), lays, "bf16")
+    _check_equal(_run_gpu(tbl, tiles, axes, "bf16", 1, 2), ref, "bf16")
