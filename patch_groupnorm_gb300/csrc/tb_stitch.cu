@@ -31,20 +31,25 @@
 // rectangular boxes by band membership (interior, width band, height band,
 // corner; times the time band in 3D).  Inside a box every element needs the
 // same set of source tiles, so one CTA takes one piece of one box (a run of
-// rows of one frame of one (batch, channel) plane) and runs a path compiled
-// for exactly that set: no per-element band tests and no divergence.
-// Threads are laid out 2D over the box: a thread keeps its columns -- and
-// so its width coefficients -- for every row it visits, and each row costs
-// one multiply-add per source address.  Loads of several rows are issued
-// before their arithmetic; 128-bit streaming loads and stores.  Each output
-// element is written once and each tile element read once: the kernel moves
-// the algorithmic minimum, all tile bytes plus all output bytes.
+// rows of the box's frame-major (frame, row) space, for one (batch, channel)
+// plane) and runs a path compiled for exactly that set: no per-element band
+// tests and no divergence.  Pieces of heavier boxes are shorter, and every
+// tile's heaviest pieces are dispatched first.  Threads are laid out 2D over
+// the box: a thread keeps its columns -- and so its width coefficients -- for
+// every row it visits, and each row costs one multiply-add per source
+// address.  On the 16-byte path each thread streams the source chunks of its
+// coming rows into its own ring of shared-memory slots with cp.async (no
+// registers held by loads in flight) and reads each node's value right before
+// its blend; stores are 128-bit streaming stores.  Each output element is
+// written once and each tile element read once: the kernel moves the
+// algorithmic minimum, all tile bytes plus all output bytes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "tb_internal.h"
 
-// Rows in flight per thread, by box kind (copy / one band / two bands / three).
+// Rows whose loads are issued together on the element path, by box kind
+// (copy / one band / two bands / three).
 #ifndef TB_STITCH_UR_COPY
 #define TB_STITCH_UR_COPY 4
 #endif
