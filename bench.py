@@ -20,7 +20,7 @@ The JSON line also carries:
               source (null if the source changed since);
   kernels     every kernel on its own workload: rotating buffer sets (no
               L2 reuse), launches replayed from a CUDA graph, CUDA events;
-  cpu_baseline  the CPU oracle timed on this host on one full step.
+  cpu_baseline  the CPU oracle timed on this host: whole steps, about 10 s.
 
 Under torchrun (N > 1) every rank runs the same step on its own GPU (weak
 scaling, no collective on the data path); the time is the max over ranks.
