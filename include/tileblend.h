@@ -86,15 +86,21 @@ typedef struct {
 } tb_axis;
 
 /*
- * Per-patch GroupNorm statistics of one (patch, sample, group) [DVA]:
- * element count, the patch's own group mean, and the sum of squared
- * deviations about that mean.  16 bytes, no padding.
+ * Partial GroupNorm statistics [DVA] of one part of the elements of one
+ * (patch, sample, group): element count, the part's own mean, and the sum of
+ * squared deviations about that mean.  16 bytes, no padding.  Each
+ * (patch, sample, group) has TB_GN_PARTS records; the statistics kernel cuts
+ * its elements into up to that many contiguous parts (how many depends on
+ * the sizes and the GPU) and gives unused records count 0.
  */
 typedef struct {
     int64_t n;
     float mean;
     float m2;
 } tb_gn_partial;
+
+/* Partial-statistics records per (patch, sample, group). */
+#define TB_GN_PARTS 8
 
 /* Largest tile count per axis, and per grid, the stitch calls accept. */
 #define TB_MAX_TILES_PER_AXIS 64
@@ -232,10 +238,13 @@ tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int64_t B, 
  * An activation [N, C, *spatial] is split along one spatial axis into P
  * patches (the ranks' shards in the pages' patch-parallel decode); patch p is
  * [N, C, *spatial_p], contiguous, with spatial[p] elements per channel.
- * Channel c belongs to group c / (C / G).  For every (p, n, g) this writes
- *   partials[(p * N + n) * G + g] = { count, mean, sum (x - mean)^2 }
- * over the C/G channels of group g in sample n of patch p (fp32
- * accumulation, deterministic order).
+ * Channel c belongs to group c / (C / G).  The C/G channels of group g in
+ * sample n of patch p are one run of elements; it is cut into up to
+ * TB_GN_PARTS contiguous parts and part k's statistics go to
+ *   partials[((p * N + n) * G + g) * TB_GN_PARTS + k]
+ *     = { count, mean, sum (x - mean)^2 }
+ * (fp32 accumulation, deterministic: the same inputs on the same GPU give
+ * the same bits).  Records of unused parts get count 0.
  *
  *   patches   host array of P device pointers
  *   P         number of patches (1 = plain, unsharded GroupNorm)
@@ -243,7 +252,8 @@ tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int64_t B, 
  *   N, C      samples and channels; C % G == 0
  *   spatial   host array of P element counts per channel (>= 0)
  *   G         number of groups (>= 1)
- *   partials  device array of P * N * G tb_gn_partial, written fully
+ *   partials  device array of P * N * G * TB_GN_PARTS tb_gn_partial,
+ *             written fully
  * Errors: TB_ERR_NULL, TB_ERR_SHAPE (C % G != 0, negative sizes, P < 1),
  * TB_ERR_UNSUPPORTED (P > 64), TB_ERR_CUDA.
  */
@@ -251,10 +261,10 @@ tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dtype dtyp
                             const int64_t* spatial, int32_t G, tb_gn_partial* partials, void* stream);
 
 /*
- * tb_patch_gn_apply -- combine the partials of all P patches into the pooled
- * group mean and the biased variance about it (divided by the total count,
- * no Bessel correction) [DVA], then normalise, apply the per-channel affine
- * and optionally SiLU:
+ * tb_patch_gn_apply -- combine the partials of all P patches (all their
+ * parts) into the pooled group mean and the biased variance about it
+ * (divided by the total count, no Bessel correction) [DVA], then normalise,
+ * apply the per-channel affine and optionally SiLU:
  *     z = (x - mean) / sqrt(var + eps) * gamma[c] + beta[c]
  *     y = silu ? z / (1 + exp(-z)) : z,   rounded once into dtype.
  * The result equals GroupNorm (+ SiLU) of the unsharded tensor.
@@ -262,8 +272,10 @@ tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dtype dtyp
  *   patches   host array of P device pointers (as tb_patch_gn_stats)
  *   outs      host array of P device pointers, same shapes; outs[p] may
  *             equal patches[p] (in place), other overlaps are not allowed
- *   partials  device array written by tb_patch_gn_stats for the same
- *             patches (P * N * G entries)
+ *   partials  device array written by tb_patch_gn_stats with the same
+ *             arguments on a GPU of the same kind (P * N * G * TB_GN_PARTS
+ *             entries; only the records that call filled are read, which
+ *             both calls derive from the arguments and the SM count)
  *   gamma     device [C] of dtype, or NULL for 1
  *   beta      device [C] of dtype, or NULL for 0
  *   eps       added to the variance (> 0 recommended; >= 0 required)
@@ -354,11 +366,13 @@ tb_status tb_gather_patches(const void* const* patches, int32_t P, const int64_t
  * partials in a fixed scratch array compiled into the library instead
  * (TB_NOALLOC_MAX_PARTIALS records of 16 bytes, 1 MiB, held on every GPU
  * that loads the library until the process exits) and allocates nothing.
+ * That holds the records of P * N * G <= TB_NOALLOC_MAX_PARTIALS /
+ * TB_GN_PARTS = 8192 (patch, sample, group) triples.
  *
  * Arguments and results are those of tb_patch_gn_apply, minus `partials`.
  * The result equals tb_patch_gn_stats followed by tb_patch_gn_apply.
  *
- *   - P * N * G larger than TB_NOALLOC_MAX_PARTIALS returns
+ *   - P * N * G * TB_GN_PARTS larger than TB_NOALLOC_MAX_PARTIALS returns
  *     TB_ERR_UNSUPPORTED and launches nothing.
  *   - The first call on each device looks up the scratch array's device
  *     address (cudaGetSymbolAddress, with that device current); make that

@@ -18,34 +18,36 @@
 //     n = nA + nB,  d = meanB - meanA,
 //     mean = meanA + d * nB / n,  M2 = M2A + M2B + d^2 * nA * nB / n.
 //
-// gn_stats_kernel: one thread-block cluster per (patch, sample, group), sized
-// to about two CTAs per SM in all.  Each thread streams 16-byte chunks through
-// a ring of cp.async slots, seven ahead.  For fp16 / bf16 it sums x - K and
+// gn_stats_kernel: each (patch, sample, group) unit's elements are cut into
+// `parts` contiguous parts (1, 2, 4 or 8: about two CTAs per SM in all), one
+// CTA per part, and every part's statistics go to their own record (the
+// apply step merges them).  Each thread streams 16-byte chunks through a
+// ring of cp.async slots, seven ahead.  For fp16 / bf16 it sums x - K and
 // (x - K)^2 over groups of 8 chunks (64 elements) on packed fp32 pairs, K
 // being the group's first element -- differences and squares of 16-bit
 // values are nearly always exact in fp32, and the shift keeps
 // M2 = S2 - S1^2 / m from cancelling -- and folds each group into its
 // running triple with Chan's update; fp32 chunks are folded one by one after
-// their own mean and M2 are computed directly.  Warps merge with shuffles,
-// warps within a CTA through shared memory, and the CTAs of the cluster
-// through distributed shared memory, in a fixed order (deterministic
-// results).
+// their own mean and M2 are computed directly.  Warps merge with shuffles and
+// then through shared memory, in a fixed order (deterministic results).
+// Earlier versions merged the CTAs of a unit in a thread-block cluster over
+// distributed shared memory into one record; the cluster's scheduling and
+// barriers cost about 1 us per launch (measured), more than the extra
+// records cost the apply step.
 //
 // Both kernels are launched with programmatic stream serialisation: their
 // parameter-only prologue may overlap the preceding kernel, and they execute
 // griddepcontrol.wait before touching global memory.
 //
-// gn_apply_kernel: one CTA per segment of one channel row.  Every warp
-// combines the P partials of its group (lane q holds patch q), forms
-// a = rstd * gamma[c] and b = beta[c] - mean * a, and the elements become
+// gn_apply_kernel: one CTA per segment of one channel row.  The CTA issues
+// its data loads, then each warp combines the P * TB_GN_PARTS records of the
+// row's group (pooled_stats) into a = rstd * gamma[c] and
+// b = beta[c] - mean * a; the elements become
 // y = silu(x * a + b), rounded once into the storage type.
-#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "tb_internal.h"
-
-namespace cg = cooperative_groups;
 
 namespace tb {
 namespace {
@@ -63,7 +65,10 @@ constexpr int STATS_SLOTS = TB_GN_STATS_SLOTS;  // cp.async ring slots per threa
 #endif
 constexpr int STATS_GROUP = TB_GN_STATS_GROUP;  // 16-bit chunks per shifted-sum group
 constexpr int APPLY_BLOCK = 128;
-constexpr int APPLY_CPT = 4;  // 16-byte chunks per thread per segment
+#ifndef TB_GN_APPLY_CPT
+#define TB_GN_APPLY_CPT 8
+#endif
+constexpr int APPLY_CPT = TB_GN_APPLY_CPT;  // 16-byte chunks per thread per segment
 
 template <int DT>
 struct GElt;
@@ -243,12 +248,10 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
     constexpr int VEC = 16 / GElt<DT>::BYTES;
     extern __shared__ __align__(16) unsigned char s_ring[];  // STATS_SLOTS x STATS_BLOCK x 16 bytes
     __shared__ Stat s_warp[STATS_BLOCK / 32];
-    __shared__ Stat s_cta;
 
-    cg::cluster_group cluster = cg::this_cluster();
-    const unsigned cs = (unsigned)p.cs;
+    const unsigned cs = (unsigned)p.parts;
     const unsigned unit = blockIdx.x / cs;
-    const int rank = (int)cluster.block_rank();
+    const int rank = (int)(blockIdx.x - unit * cs);
     const unsigned NG = (unsigned)p.N * (unsigned)p.G;
     const unsigned pp = unit / NG;
     const unsigned rem = unit - pp * NG;
@@ -328,7 +331,8 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
         }
     }
 
-    // warp, then CTA (fixed order), then cluster (fixed order)
+    // warp, then CTA (fixed order); the part's record, and the empty records
+    // of parts no CTA takes (records rank + j * cs, j >= 1)
     acc = warp_reduce(acc);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) s_warp[warp] = acc;
@@ -337,41 +341,91 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
         Stat t = s_warp[0];
 #pragma unroll
         for (int w = 1; w < STATS_BLOCK / 32; ++w) t = chan(t, s_warp[w]);
-        s_cta = t;
-    }
-    cluster.sync();
-    if (rank == 0 && threadIdx.x == 0) {
-        Stat t = s_cta;
-        for (int r = 1; r < (int)cs; ++r) t = chan(t, *cluster.map_shared_rank(&s_cta, r));
+        int64_t count;
+        if constexpr (VECTOR) {
+            const int64_t nv = len / VEC;
+            count = (nv * (rank + 1) / cs - nv * rank / cs) * VEC;
+        } else {
+            count = len * (rank + 1) / cs - len * rank / cs;
+        }
+        GnPartial* const rec = p.partials + (int64_t)unit * TB_GN_PARTS;
         GnPartial out;
-        out.n = len;
-        out.mean = len > 0 ? t.mean : 0.f;
-        out.m2 = len > 0 ? t.m2 : 0.f;
-        p.partials[unit] = out;
+        out.n = count;
+        out.mean = count > 0 ? t.mean : 0.f;
+        out.m2 = count > 0 ? t.m2 : 0.f;
+        rec[rank] = out;
+        const GnPartial none = {0, 0.f, 0.f};
+        for (int k = rank + (int)cs; k < TB_GN_PARTS; k += (int)cs) rec[k] = none;
     }
-    cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
 
-// Pooled (mean, rstd) of group g of sample n from the P partials; every
-// lane of the warp returns the same values.
+// Pooled (mean, rstd) of group g of sample n from the part records, computed
+// by one warp.  The statistics kernel filled the first `parts` records of
+// every (patch, sample, group) and left the rest empty, so only those are
+// read.  Each record (count c, mean m, M2) adds
+// c, c * (m - K) and M2 + c * (m - K)^2 to three sums taken about K, the mean
+// of the first record with elements (so the sums do not cancel); then
+//     mean = K + S1 / n,   M2 = S2 - S1^2 / n   (Chan's combination, summed),
+// and the variance is M2 / n, biased.  Lane 0 holds the result.
 __device__ __forceinline__ void pooled_stats(const GnApplyParams& p, int64_t n, int64_t g, float& mean, float& rstd) {
     const int lane = threadIdx.x & 31;
-    Stat s{0.f, 0.f, 0.f};
-    for (int q = lane; q < p.P; q += 32) {
-        const GnPartial* src = p.partials + ((int64_t)q * p.N + n) * p.G + g;
+    const int total = p.P * p.parts;  // parts beyond p.parts hold no elements
+    auto record = [&](int q, float& c, float& m, float& m2) {
+        const int pq = q / p.parts, k = q - pq * p.parts;
+        const GnPartial* src = p.partials + (((int64_t)pq * p.N + n) * p.G + g) * TB_GN_PARTS + k;
         const longlong2 raw = __ldg(reinterpret_cast<const longlong2*>(src));
-        const float pm = __int_as_float((int)(raw.y & 0xffffffffLL));
-        const float pm2 = __int_as_float((int)(raw.y >> 32));
-        s = chan(s, Stat{(float)raw.x, pm, pm2});
+        c = (float)raw.x;
+        m = __int_as_float((int)(raw.y & 0xffffffffLL));
+        m2 = __int_as_float((int)(raw.y >> 32));
+    };
+    // the first 32 records stay in registers (all of them when P <= 4)
+    float c0 = 0.f, m0 = 0.f, v0 = 0.f;
+    if (lane < total) record(lane, c0, m0, v0);
+    float K = 0.f;
+    unsigned has = __ballot_sync(0xffffffffu, c0 > 0.f);
+    if (has != 0u) {
+        K = __shfl_sync(0xffffffffu, m0, __ffs(has) - 1);
+    } else {
+        for (int base = 32; base < total; base += 32) {
+            float c = 0.f, m = 0.f, m2 = 0.f;
+            if (base + lane < total) record(base + lane, c, m, m2);
+            has = __ballot_sync(0xffffffffu, c > 0.f);
+            if (has != 0u) {
+                K = __shfl_sync(0xffffffffu, m, __ffs(has) - 1);
+                break;
+            }
+        }
     }
-    s = warp_reduce(s);
-    const float tn = __shfl_sync(0xffffffffu, s.n, 0);
-    const float tm = __shfl_sync(0xffffffffu, s.mean, 0);
-    const float tm2 = __shfl_sync(0xffffffffu, s.m2, 0);
-    const float var = tn > 0.f ? tm2 / tn : 0.f;  // biased: divide by the count
-    mean = tm;
+    float sn = 0.f, s1 = 0.f, s2 = 0.f;
+    auto add = [&](float c, float m, float m2) {
+        if (c > 0.f) {
+            const float d = m - K;
+            sn += c;
+            s1 = fmaf(c, d, s1);
+            s2 += fmaf(c * d, d, m2);
+        }
+    };
+    add(c0, m0, v0);
+    for (int q = lane + 32; q < total; q += 32) {
+        float c, m, m2;
+        record(q, c, m, m2);
+        add(c, m, m2);
+    }
+#pragma unroll
+    for (int delta = 16; delta >= 1; delta >>= 1) {  // fixed order: deterministic
+        sn += __shfl_down_sync(0xffffffffu, sn, delta);
+        s1 += __shfl_down_sync(0xffffffffu, s1, delta);
+        s2 += __shfl_down_sync(0xffffffffu, s2, delta);
+    }
+    const float q1 = sn > 0.f ? s1 / sn : 0.f;
+    const float var = sn > 0.f ? fmaxf(0.f, fmaf(-s1, q1, s2) / sn) : 0.f;  // biased: divide by the count
+    mean = K + q1;
     rstd = 1.0f / sqrtf(var + p.eps);
 }
+
+// (a, b) with y = x * a + b for channel c.
+template <int DT>
+__device__ __forceinline__ float2 channel_affine(const GnApplyParams& p, int64_t n, int64_t g, int64_t c);
 
 template <int DT>
 __device__ __forceinline__ float load_param(const void* ptr, int64_t c, float dflt) {
@@ -381,6 +435,18 @@ __device__ __forceinline__ float load_param(const void* ptr, int64_t c, float df
     } else {
         return GElt<DT>::to_f(__ldg(reinterpret_cast<const unsigned short*>(ptr) + c));
     }
+}
+
+template <int DT>
+__device__ __forceinline__ float2 channel_affine(const GnApplyParams& p, int64_t n, int64_t g, int64_t c) {
+    // every warp combines the records itself: a few loads and shuffles,
+    // cheaper than a CTA barrier (measured)
+    float mean, rstd;
+    pooled_stats(p, n, g, mean, rstd);
+    mean = __shfl_sync(0xffffffffu, mean, 0);
+    rstd = __shfl_sync(0xffffffffu, rstd, 0);
+    const float a = rstd * load_param<DT>(p.gamma, c, 1.f);
+    return make_float2(a, load_param<DT>(p.beta, c, 0.f) - mean * a);
 }
 
 // silu(z) = z / (1 + e^-z), with e^-z = 2^(-z log2 e) and the reciprocal
@@ -442,10 +508,8 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
             const int idx = threadIdx.x + q * APPLY_BLOCK;
             if (idx < nchunk) v[q] = __ldcs(src + idx);
         }
-        float mean, rstd;
-        pooled_stats(p, n, g, mean, rstd);
-        const float a = rstd * load_param<DT>(p.gamma, c, 1.f);
-        const float b = load_param<DT>(p.beta, c, 0.f) - mean * a;
+        const float2 ab = channel_affine<DT>(p, n, g, c);
+        const float a = ab.x, b = ab.y;
 #pragma unroll
         for (int q = 0; q < APPLY_CPT; ++q) {
             const int idx = threadIdx.x + q * APPLY_BLOCK;
@@ -469,10 +533,8 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
             __stcs(dst + idx, o);
         }
     } else {
-        float mean, rstd;
-        pooled_stats(p, n, g, mean, rstd);
-        const float a = rstd * load_param<DT>(p.gamma, c, 1.f);
-        const float b = load_param<DT>(p.beta, c, 0.f) - mean * a;
+        const float2 ab = channel_affine<DT>(p, n, g, c);
+        const float a = ab.x, b = ab.y;
         const void* src = p.patches[pp];
         void* dst = p.outs[pp];
         for (int64_t e = e_begin + threadIdx.x; e < e_end; e += APPLY_BLOCK) {
@@ -502,24 +564,16 @@ cudaError_t stats_dt(const GnStatsParams& p, int64_t units, cudaStream_t s) {
                                              (int)stats_smem(p.aligned != 0));
         if (e != cudaSuccess) return e;
     }
-    if (p.cs > 8) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(units * p.cs), 1, 1);
+    cfg.gridDim = dim3((unsigned)(units * p.parts), 1, 1);
     cfg.blockDim = dim3(STATS_BLOCK, 1, 1);
     cfg.dynamicSmemBytes = stats_smem(p.aligned != 0);
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
 

@@ -40,9 +40,10 @@
 #ifndef TB_RAMP_MAX_ROWS_PER_THREAD
 #define TB_RAMP_MAX_ROWS_PER_THREAD 16
 #endif
-// Cluster size of the GroupNorm statistics kernel; 0 picks it from occupancy.
-#ifndef TB_GN_FORCE_CS
-#define TB_GN_FORCE_CS 0
+// CTAs per GroupNorm statistics unit (a power of two dividing TB_GN_PARTS);
+// 0 picks it from the sizes and the SM count.
+#ifndef TB_GN_FORCE_PARTS
+#define TB_GN_FORCE_PARTS 0
 #endif
 
 static_assert(tb::RAMP_MAXCOVER == TB_RAMP_MAX_COVER, "ramp cover limit differs from the header");
@@ -317,7 +318,30 @@ tb_status gn_validate(const void* const* patches, int32_t P, tb_dtype dtype, int
             return TB_ERR_SHAPE;
     }
     if (N > 0 && C > 0 && partials == nullptr) return TB_ERR_NULL;
-    if ((double)P * (double)N * (double)G > 2.0e9) return TB_ERR_UNSUPPORTED;
+    if ((double)P * (double)N * (double)G * TB_GN_PARTS > 2.0e9) return TB_ERR_UNSUPPORTED;
+    return TB_OK;
+}
+
+// CTAs per GroupNorm statistics unit, which is also the number of records
+// per (patch, sample, group) the statistics kernel fills: 1, 2, 4 or 8
+// (dividing TB_GN_PARTS), about two CTAs per SM in all, each streaming
+// >= 16 KB.  Measured on GB300: more, shorter CTAs per unit lose more to
+// their fixed costs than they gain.  Both GroupNorm calls derive it from the
+// same arguments, so the apply step reads exactly the records filled.
+tb_status gn_parts(int32_t P, int64_t N, int64_t C, const int64_t* spatial, int32_t G, tb_dtype dtype, int* parts) {
+    int64_t max_len = 0;
+    for (int p = 0; p < P; ++p) max_len = std::max(max_len, (C / G) * spatial[p]);
+    const int64_t units = (int64_t)P * N * G;
+    const int64_t bytes = max_len * elem_bytes(dtype);
+    int sms = 0;
+    tb_status s = device_sms(&sms);
+    if (s != TB_OK) return s;
+    int64_t want = units > 0 ? (2LL * sms + units / 2) / units : 1;
+    want = std::min<int64_t>(want, bytes / 16384);
+    int k = 1;
+    while (k * 2 <= TB_GN_PARTS && k * 2 <= want) k *= 2;
+    if (TB_GN_FORCE_PARTS > 0) k = TB_GN_FORCE_PARTS;
+    *parts = k;
     return TB_OK;
 }
 
@@ -630,12 +654,10 @@ TB_API tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dty
     const int vec = 16 / elem_bytes(dtype);
     const int64_t cg = C / G;
     bool aligned = true;
-    int64_t max_len = 0;
     for (int p = 0; p < P; ++p) {
         prm.patches[p] = patches[p];
         prm.spatial[p] = spatial[p];
         const int64_t len = cg * spatial[p];
-        max_len = std::max(max_len, len);
         if (spatial[p] > 0 && (!aligned16(patches[p]) || len % vec != 0)) aligned = false;
     }
     prm.partials = reinterpret_cast<tb::GnPartial*>(partials);
@@ -644,20 +666,12 @@ TB_API tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dty
     prm.P = P;
     prm.G = G;
     prm.aligned = aligned ? 1 : 0;
-    // CTAs per unit (the cluster size, 1..8): about two CTAs per SM in all,
-    // each streaming >= 16 KB.  Measured on GB300: larger clusters of
-    // shorter CTAs lose more to their barriers than they gain in parallelism.
     const int64_t units = (int64_t)P * N * G;
-    const int64_t bytes = max_len * elem_bytes(dtype);
-    int sms = 0;
-    s = device_sms(&sms);
+    int parts = 1;
+    s = gn_parts(P, N, C, spatial, G, dtype, &parts);
     if (s != TB_OK) return s;
-    int64_t cs64 = units > 0 ? (2LL * sms + units / 2) / units : 1;
-    cs64 = std::min<int64_t>(cs64, bytes / 16384);
-    int cs = (int)std::max<int64_t>(1, std::min<int64_t>(8, cs64));
-    if (TB_GN_FORCE_CS > 0) cs = TB_GN_FORCE_CS;
-    prm.cs = cs;
-    if (units * cs > 2147483647LL) return TB_ERR_UNSUPPORTED;
+    prm.parts = parts;
+    if (units * parts > 2147483647LL) return TB_ERR_UNSUPPORTED;
     cudaError_t e = tb::launch_gn_stats(prm, (int)dtype, units, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return TB_OK;
@@ -702,6 +716,10 @@ TB_API tb_status tb_patch_gn_apply(const void* const* patches, void* const* outs
     prm.P = P;
     prm.G = G;
     prm.seg = (int32_t)seg;
+    int parts = 1;
+    s = gn_parts(P, N, C, spatial, G, dtype, &parts);
+    if (s != TB_OK) return s;
+    prm.parts = parts;
     prm.eps = eps;
     prm.silu = silu ? 1 : 0;
     prm.aligned = aligned ? 1 : 0;

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "tileblend.h"
+
 namespace tb {
 
 enum Dtype : int32_t { F32 = 0, F16 = 1, BF16 = 2 };
@@ -223,13 +225,16 @@ struct GnPartial {  // layout-identical to tb_gn_partial
 };
 static_assert(sizeof(GnPartial) == 16, "partial must be 16 bytes");
 
+static_assert(TB_GN_PARTS >= 1 && TB_GN_PARTS <= 32 && (TB_GN_PARTS & (TB_GN_PARTS - 1)) == 0,
+              "records per unit must be a power of two");
+
 struct GnStatsParams {
     const void* patches[GN_MAXP];
     int64_t spatial[GN_MAXP];     // elements per channel in patch p
     GnPartial* partials;          // [P][N][G]
     int64_t N, C;
     int32_t P, G;
-    int32_t cs;                   // CTAs per (p, n, g) unit (cluster size)
+    int32_t parts;                // CTAs per (p, n, g) unit: 1, 2, 4 or 8 (divides TB_GN_PARTS)
     int32_t aligned;              // every unit start and length is a multiple of the vector width
 };
 
@@ -245,6 +250,7 @@ struct GnApplyParams {
     int64_t N, C;
     int32_t P, G;
     int32_t seg;                      // elements per segment
+    int32_t parts;                    // records per (p, n, g) the statistics kernel filled
     float eps;
     int32_t silu;
     int32_t aligned;                  // every channel row start is 16-byte aligned

@@ -8,7 +8,8 @@
 // kernels and their arguments are otherwise the existing ones.
 //
 // The array holds TB_NOALLOC_MAX_PARTIALS 16-byte records (1 MiB) on every
-// device that loads the library, for the life of the process.  Calls share
+// device that loads the library, for the life of the process: the
+// TB_GN_PARTS records of each of up to 8192 (patch, sample, group) units.  Calls share
 // it: each call's statistics kernel writes every record its apply kernel
 // reads, so nothing needs clearing between calls, but calls whose work
 // overlaps on the GPU race on it.
@@ -59,7 +60,7 @@ TB_API tb_status tb_patch_group_norm_noalloc(const void* const* patches, void* c
                                              const void* gamma, const void* beta, float eps, int32_t silu,
                                              void* stream) {
     if (P < 1 || N < 0 || C < 0 || G < 1) return TB_ERR_SHAPE;
-    if ((double)P * (double)N * (double)G > (double)TB_NOALLOC_MAX_PARTIALS) return TB_ERR_UNSUPPORTED;
+    if ((double)P * (double)N * (double)G * TB_GN_PARTS > (double)TB_NOALLOC_MAX_PARTIALS) return TB_ERR_UNSUPPORTED;
     // checks the apply step would make, done before the statistics launch
     if (!(eps >= 0.0f) || eps > 3.0e38f) return TB_ERR_SHAPE;
     if (outs == nullptr) return TB_ERR_NULL;

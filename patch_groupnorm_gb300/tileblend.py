@@ -36,6 +36,7 @@ TB_OK, TB_ERR_NULL, TB_ERR_DTYPE, TB_ERR_SHAPE, TB_ERR_GEOMETRY, TB_ERR_UNSUPPOR
 TB_F32, TB_F16, TB_BF16 = 0, 1, 2
 TB_MAX_TILES_PER_AXIS = 64
 TB_MAX_TILES = 1024
+TB_GN_PARTS = 8
 
 _DTYPES = {torch.float32: TB_F32, torch.float16: TB_F16, torch.bfloat16: TB_BF16}
 
@@ -334,18 +335,20 @@ def _gn_args(patches: Sequence[torch.Tensor]) -> Tuple[int, int, int, list, list
 
 
 def new_partials(P: int, N: int, G: int, device=None) -> torch.Tensor:
-    """Device buffer for P * N * G tb_gn_partial records (16 bytes each)."""
-    return torch.empty((P, N, G, 2), dtype=torch.int64, device=device or torch.device("cuda"))
+    """Device buffer for the P * N * G * TB_GN_PARTS tb_gn_partial records
+    (16 bytes each) that tb_patch_gn_stats writes."""
+    return torch.empty((P, N, G, TB_GN_PARTS, 2), dtype=torch.int64, device=device or torch.device("cuda"))
 
 
 def tb_patch_gn_stats(patches: Sequence[torch.Tensor], G: int, partials: torch.Tensor, stream=None) -> torch.Tensor:
-    """Per-patch (count, mean, M2) of every (sample, group) into ``partials``
-    (a [P, N, G, 2] int64 buffer from ``new_partials``)."""
+    """(count, mean, M2) of every part of every (patch, sample, group) into
+    ``partials`` (a [P, N, G, TB_GN_PARTS, 2] int64 buffer from
+    ``new_partials``)."""
     N, C, dt, spatial, ptrs = _gn_args(patches)
     P = len(patches)
     _cuda_contig(partials, "partials")
-    if partials.numel() * partials.element_size() != P * N * G * 16:
-        raise ValueError("partials must hold P*N*G 16-byte records")
+    if partials.numel() * partials.element_size() != P * N * G * TB_GN_PARTS * 16:
+        raise ValueError("partials must hold P*N*G*TB_GN_PARTS 16-byte records")
     sp = (ctypes.c_int64 * P)(*spatial)
     _check(_lib.tb_patch_gn_stats(_ptr_array(ptrs), P, dt, N, C, sp, G, partials.data_ptr(), _stream_handle(stream)),
            "tb_patch_gn_stats")
@@ -373,8 +376,8 @@ def tb_patch_gn_apply(patches: Sequence[torch.Tensor], outs: Sequence[torch.Tens
             if v.numel() != C or v.dtype != patches[0].dtype:
                 raise ValueError("%s must be [C] of the patches' dtype" % name)
     _cuda_contig(partials, "partials")
-    if partials.numel() * partials.element_size() != P * N * G * 16:
-        raise ValueError("partials must hold P*N*G 16-byte records")
+    if partials.numel() * partials.element_size() != P * N * G * TB_GN_PARTS * 16:
+        raise ValueError("partials must hold P*N*G*TB_GN_PARTS 16-byte records")
     sp = (ctypes.c_int64 * P)(*spatial)
     _check(_lib.tb_patch_gn_apply(_ptr_array(ptrs), _ptr_array(optrs), P, dt, N, C, sp, G, partials.data_ptr(),
                                   gamma.data_ptr() if gamma is not None else None,
@@ -400,9 +403,9 @@ def tb_patch_group_norm_noalloc(patches: Sequence[torch.Tensor], outs: Sequence[
                                 gamma: Optional[torch.Tensor], beta: Optional[torch.Tensor], eps: float,
                                 silu: bool = True, stream=None) -> Sequence[torch.Tensor]:
     """PatchGroupNorm for callers that cannot allocate device memory: the
-    partial statistics live in the library's own fixed scratch array
-    (at most TB_NOALLOC_MAX_PARTIALS = P * N * G records), so the call needs
-    no buffer besides the inputs and outputs.  Calls share that array: order
+    partial statistics live in the library's own fixed scratch array (room
+    for P * N * G * TB_GN_PARTS <= TB_NOALLOC_MAX_PARTIALS records), so the
+    call needs no buffer besides the inputs and outputs.  Calls share that array: order
     them on one stream.  The first call on a device looks the array up; make
     it before any stream capture."""
     N, C, dt, spatial, ptrs = _gn_args(patches)

@@ -98,14 +98,19 @@ def test_full_workload_within_tolerance_and_not_the_broken_variants(tbl, name):
 def test_partials_match_oracle(tbl, dtype):
     patches, _, _ = synth.groupnorm_patches(3, (2, 24, 37, 16), 2, 3, (-3.0, 0.5, 2.0), dtype)
     _, part = run_gpu(tbl, patches, 6, None, None, 1e-6, True)
-    part = part.view(-1, 2).numpy()
-    cnt = part[:, 0]
-    packed = np.ascontiguousarray(part[:, 1]).view(np.float32)
-    mean, m2 = packed[0::2], packed[1::2]
+    part = part.view(-1, tbl.TB_GN_PARTS, 2).numpy()
+    cnt = part[..., 0].astype(np.float64)
+    packed = np.ascontiguousarray(part[..., 1]).view(np.float32).reshape(part.shape[0], tbl.TB_GN_PARTS, 2)
+    mean, m2 = packed[..., 0].astype(np.float64), packed[..., 1].astype(np.float64)
+    # merge each unit's parts: pooled count, mean, and M2 about the pooled mean
+    n = cnt.sum(axis=1)
+    mu = (cnt * mean).sum(axis=1) / n
+    M2 = (m2 + cnt * (mean - mu[:, None]) ** 2).sum(axis=1)
+    assert ((cnt > 0) | ((mean == 0) & (m2 == 0))).all()      # unused parts are empty records
     oc, om, om2 = GN.patch_partials([_f64(p) for p in patches], 6)
-    assert np.array_equal(cnt, oc.reshape(-1))
-    assert np.abs(mean - om.reshape(-1)).max() <= 2e-5 * np.maximum(1, np.abs(om)).max()
-    assert np.abs(m2 / om2.reshape(-1) - 1).max() <= 2e-5
+    assert np.array_equal(n, oc.reshape(-1))
+    assert np.abs(mu - om.reshape(-1)).max() <= 2e-5 * np.maximum(1, np.abs(om)).max()
+    assert np.abs(M2 / om2.reshape(-1) - 1).max() <= 2e-5
 
 
 def test_stats_deterministic(tbl):
@@ -170,8 +175,9 @@ def test_empty_patch_and_empty_batch(tbl):
     torch.cuda.synchronize()
 
 
-def test_large_group_spans_a_cluster(tbl):
-    # one big group per sample: every unit is split over a cluster of CTAs
+def test_large_group_spans_several_ctas(tbl):
+    # one big group per sample: every unit is split over several CTAs, each
+    # writing its own part record
     patches, gamma, beta = synth.groupnorm_patches(9, (1, 8, 512, 512), 2, 2, (-3, 3), "bf16")
     outs, _ = run_gpu(tbl, patches, 1, gamma, beta, 1e-6, True)
     with np.errstate(over="ignore"):

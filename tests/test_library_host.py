@@ -245,3 +245,10 @@ def test_patchify_and_gather_reject_before_launch(tbl):
     # any sizes, not only whole bands, as long as they sum to the axis
     odd = (ctypes.c_int64 * 3)(1, 0, 207)
     assert gather((ctypes.c_void_p * 3)(16, None, 48), 3, odd, 2, 5, empty, 4, 0, 16, None) == tbl.TB_OK
+
+
+def test_header_constants_match_the_binding(tbl):
+    src = open(HEADER).read()
+    for name in ("TB_MAX_TILES_PER_AXIS", "TB_MAX_TILES", "TB_GN_PARTS", "TB_NOALLOC_MAX_PARTIALS", "TB_MAX_PATCHES"):
+        m = re.search(r"#define\s+%s\s+(\d+)" % name, src)
+        assert m and int(m.group(1)) == getattr(tbl, name), name
