@@ -15,10 +15,10 @@
 // narrowed to fp32 (the same page divides in float64 so that on-device
 // coefficients equal Python's), computed here once per distinct e.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <mutex>
 
 #include "tb_internal.h"
 #include "tileblend.h"
@@ -121,21 +121,23 @@ bool bands_apart(const Axis& g) {
 // ---------------------------------------------------------------------------
 
 constexpr int MAX_DEVICES = 64;
-int g_sm_count[MAX_DEVICES] = {};
-std::mutex g_mu;
+std::atomic<int> g_sm_count[MAX_DEVICES] = {};  // 0: not looked up yet
 
 tb_status device_sms(int* sms) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (dev >= 0 && dev < MAX_DEVICES && g_sm_count[dev] > 0) {
-        *sms = g_sm_count[dev];
-        return TB_OK;
+    if (dev >= 0 && dev < MAX_DEVICES) {
+        const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (cached > 0) {
+            *sms = cached;
+            return TB_OK;
+        }
     }
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (dev >= 0 && dev < MAX_DEVICES) g_sm_count[dev] = n;
+    if (dev >= 0 && dev < MAX_DEVICES) g_sm_count[dev].store(n, std::memory_order_relaxed);
     *sms = n;
     return TB_OK;
 }
