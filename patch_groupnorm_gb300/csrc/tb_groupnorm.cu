@@ -249,9 +249,9 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
     extern __shared__ __align__(16) unsigned char s_ring[];  // STATS_SLOTS x STATS_BLOCK x 16 bytes
     __shared__ Stat s_warp[STATS_BLOCK / 32];
 
-    const unsigned cs = (unsigned)p.parts;
-    const unsigned unit = blockIdx.x / cs;
-    const int rank = (int)(blockIdx.x - unit * cs);
+    const unsigned parts = (unsigned)p.parts;
+    const unsigned unit = blockIdx.x / parts;
+    const int rank = (int)(blockIdx.x - unit * parts);
     const unsigned NG = (unsigned)p.N * (unsigned)p.G;
     const unsigned pp = unit / NG;
     const unsigned rem = unit - pp * NG;
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
         // thread streams its chunks through its own ring of STATS_SLOTS
         // shared-memory slots with cp.async, STATS_SLOTS - 1 chunks ahead.
         const int64_t nv = len / VEC;
-        const int64_t v0 = nv * rank / cs, v1 = nv * (rank + 1) / cs;
+        const int64_t v0 = nv * rank / parts, v1 = nv * (rank + 1) / parts;
         const uint4* src = reinterpret_cast<const uint4*>(base);
         const int64_t first = v0 + threadIdx.x;
         const int cnt = first < v1 ? (int)((v1 - first + STATS_BLOCK - 1) / STATS_BLOCK) : 0;
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
         }
         cp_async_wait<0>();
     } else {
-        const int64_t e0 = len * rank / cs, e1 = len * (rank + 1) / cs;
+        const int64_t e0 = len * rank / parts, e1 = len * (rank + 1) / parts;
         for (int64_t e = e0 + threadIdx.x; e < e1; e += STATS_BLOCK) {
             const float x = load_scalar<DT>(base, e);
             acc = chan(acc, Stat{1.f, x, 0.f});
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
     }
 
     // warp, then CTA (fixed order); the part's record, and the empty records
-    // of parts no CTA takes (records rank + j * cs, j >= 1)
+    // of parts no CTA takes (records rank + j * parts, j >= 1)
     acc = warp_reduce(acc);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) s_warp[warp] = acc;
@@ -344,9 +344,9 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
         int64_t count;
         if constexpr (VECTOR) {
             const int64_t nv = len / VEC;
-            count = (nv * (rank + 1) / cs - nv * rank / cs) * VEC;
+            count = (nv * (rank + 1) / parts - nv * rank / parts) * VEC;
         } else {
-            count = len * (rank + 1) / cs - len * rank / cs;
+            count = len * (rank + 1) / parts - len * rank / parts;
         }
         GnPartial* const rec = p.partials + (int64_t)unit * TB_GN_PARTS;
         GnPartial out;
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
         out.m2 = count > 0 ? t.m2 : 0.f;
         rec[rank] = out;
         const GnPartial none = {0, 0.f, 0.f};
-        for (int k = rank + (int)cs; k < TB_GN_PARTS; k += (int)cs) rec[k] = none;
+        for (int k = rank + (int)parts; k < TB_GN_PARTS; k += (int)parts) rec[k] = none;
     }
 }
 
