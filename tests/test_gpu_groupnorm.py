@@ -182,3 +182,13 @@ def test_large_group_spans_several_ctas(tbl):
     outs, _ = run_gpu(tbl, patches, 1, gamma, beta, 1e-6, True)
     with np.errstate(over="ignore"):
         assert check_outputs(outs, patches, gamma, beta, 1, 1e-6, True, "bf16") <= 1.0
+
+
+def test_largest_patch_count(tbl):
+    # 64 patches (the most one call takes), one height row each, ragged widths of data per group
+    x = torch.randn(2, 16, 64, 24, generator=torch.Generator().manual_seed(64), dtype=torch.float64)
+    parts = [(x[:, :, r:r + 1] + (r % 7 - 3)).to(torch.bfloat16) for r in range(64)]
+    outs, part = run_gpu(tbl, parts, 4, None, None, 1e-6, True)
+    assert part.numel() * 8 == 64 * 2 * 4 * tbl.TB_GN_PARTS * 16
+    with np.errstate(over="ignore"):
+        assert check_outputs(outs, parts, None, None, 4, 1e-6, True, "bf16") <= 1.0
