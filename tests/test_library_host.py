@@ -252,3 +252,30 @@ def test_header_constants_match_the_binding(tbl):
     for name in ("TB_MAX_TILES_PER_AXIS", "TB_MAX_TILES", "TB_GN_PARTS", "TB_NOALLOC_MAX_PARTIALS", "TB_MAX_PATCHES"):
         m = re.search(r"#define\s+%s\s+(\d+)" % name, src)
         assert m and int(m.group(1)) == getattr(tbl, name), name
+
+
+def test_product_path_and_oracle_share_no_code():
+    # the package never imports the oracle, and the oracle never imports the
+    # package or links the library; only tests, the smoke check and the
+    # benchmark's CPU legs bring the two together
+    import ast
+    import glob
+
+    def imports(path):
+        tree = ast.parse(open(path).read())
+        names = set()
+        for node in ast.walk(tree):
+            if isinstance(node, ast.Import):
+                names.update(a.name.split(".")[0] for a in node.names)
+            elif isinstance(node, ast.ImportFrom) and node.module:
+                names.add(node.module.split(".")[0])
+        return names
+
+    for path in glob.glob(os.path.join(ROOT, "patch_groupnorm_gb300", "*.py")):
+        assert "oracle" not in imports(path), path
+    for path in glob.glob(os.path.join(ROOT, "oracle", "*.py")):
+        assert "patch_groupnorm_gb300" not in imports(path), path
+    for path in glob.glob(os.path.join(ROOT, "oracle", "*.c")) + glob.glob(os.path.join(ROOT, "oracle", "*.py")):
+        assert "tileblend" not in open(path).read(), path
+    for path in glob.glob(os.path.join(ROOT, "patch_groupnorm_gb300", "csrc", "*")):
+        assert "oracle" not in open(path).read().lower(), path
