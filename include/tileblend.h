@@ -255,7 +255,8 @@ tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int64_t B, 
  *   partials  device array of P * N * G * TB_GN_PARTS tb_gn_partial,
  *             written fully
  * Errors: TB_ERR_NULL, TB_ERR_SHAPE (C % G != 0, negative sizes, P < 1),
- * TB_ERR_UNSUPPORTED (P > 64), TB_ERR_CUDA.
+ * TB_ERR_UNSUPPORTED (P > 64, or P * N * G * TB_GN_PARTS above 2e9),
+ * TB_ERR_CUDA.
  */
 tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dtype dtype, int64_t N, int64_t C,
                             const int64_t* spatial, int32_t G, tb_gn_partial* partials, void* stream);
