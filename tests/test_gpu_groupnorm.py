@@ -192,3 +192,30 @@ def test_largest_patch_count(tbl):
     assert part.numel() * 8 == 64 * 2 * 4 * tbl.TB_GN_PARTS * 16
     with np.errstate(over="ignore"):
         assert check_outputs(outs, parts, None, None, 4, 1e-6, True, "bf16") <= 1.0
+
+
+def test_guard_bands_and_inputs_untouched(tbl):
+    # outputs and partials sit between canary bands; inputs are read only
+    patches, gamma, beta = synth.groupnorm_patches(65, (2, 32, 20, 36), 3, 3, (-3.0, 0.0, 3.0), "bf16")
+    dev = [p.cuda() for p in patches]
+    keep = [p.clone() for p in dev]
+    guard = 4096
+    bufs, outs = [], []
+    for p in dev:
+        buf = torch.full((p.numel() + 2 * guard,), 77.0, dtype=torch.bfloat16, device="cuda")
+        bufs.append(buf)
+        outs.append(buf[guard:guard + p.numel()].view(p.shape))
+    P, N, G = len(dev), dev[0].shape[0], 4
+    n_rec = P * N * G * tbl.TB_GN_PARTS
+    pbuf = torch.full((2 * n_rec + 2 * guard,), -5, dtype=torch.int64, device="cuda")
+    part = pbuf[guard:guard + 2 * n_rec].view(P, N, G, tbl.TB_GN_PARTS, 2)
+    tbl.tb_patch_gn_stats(dev, G, part)
+    tbl.tb_patch_gn_apply(dev, outs, G, part, gamma.cuda(), beta.cuda(), 1e-6, True)
+    torch.cuda.synchronize()
+    for buf, p in zip(bufs, dev):
+        assert (buf[:guard] == 77.0).all() and (buf[guard + p.numel():] == 77.0).all()
+    assert (pbuf[:guard] == -5).all() and (pbuf[guard + 2 * n_rec:] == -5).all()
+    for p, k in zip(dev, keep):
+        assert torch.equal(p, k)
+    with np.errstate(over="ignore"):
+        assert check_outputs([o.cpu() for o in outs], patches, gamma, beta, G, 1e-6, True, "bf16") <= 1.0
