@@ -156,3 +156,16 @@ def test_split_feeds_patch_group_norm(tbl):
     got = whole.double().cpu().numpy()
     ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -8))) - 7)
     assert (np.abs(got - ref) <= ulp).all()
+
+
+def test_gather_writes_nothing_outside_its_output(tbl):
+    shape = (2, 3, 37, 40)
+    x = synth.normal_tensor(77, shape, "bf16").cuda()
+    parts = tbl.tb_patchify(x, 2, 1, 5)
+    guard = 4096
+    buf = torch.full((x.numel() + 2 * guard,), 9.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + x.numel()].view(shape)
+    tbl.tb_gather_patches(parts, [p.shape[2] for p in parts], 2, out=out)
+    torch.cuda.synchronize()
+    assert (buf[:guard] == 9.0).all() and (buf[guard + x.numel():] == 9.0).all()
+    assert np.array_equal(_bits(out), _bits(x))
