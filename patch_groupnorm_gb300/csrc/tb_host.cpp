@@ -518,7 +518,7 @@ tb_status ramp_axis(const tb_ramp_axis* a, int gran, tb::RampAxisK& k) {
 // C ABI
 // ===========================================================================
 
-TB_API size_t tb_version(void) { return 10000 * 0 + 100 * 1 + 0; }
+TB_API size_t tb_version(void) { return 10000 * 0 + 100 * 2 + 0; }
 
 TB_API const char* tb_status_string(tb_status s) {
     switch (s) {
