@@ -91,7 +91,11 @@ typedef struct {
  * squared deviations about that mean.  16 bytes, no padding.  Each
  * (patch, sample, group) has TB_GN_PARTS records; the statistics kernel cuts
  * its elements into up to that many contiguous parts (how many depends on
- * the sizes and the GPU) and gives unused records count 0.
+ * the sizes and the GPU) and gives the unused records count 0.  A record
+ * describes itself: the apply step reads all TB_GN_PARTS records of every
+ * unit and merges those with a nonzero count, so record sets from different
+ * statistics calls (other patch counts, other GPUs, other ranks) combine
+ * freely.
  */
 typedef struct {
     int64_t n;
@@ -184,6 +188,100 @@ tb_status tb_stitch3d(const void* const* tiles, tb_dtype dtype, int64_t B, int64
                       int64_t out_w, void* stream);
 
 /*
+ * Row-sharded stitch [DVA], the halo-exchange commits: the tile rows of the
+ * height axis are shared out among `world` ranks, each rank decodes and
+ * stitches its own rows, and before stitching, rank r receives from rank
+ * r - 1 the raw rows its first tile row blends with: the last e_y(row_begin)
+ * rows of every tile of rank r - 1's last tile row (one message per rank
+ * boundary).  The ranks' outputs, concatenated in rank order along the
+ * height, equal the unsharded stitch bit for bit.
+ *
+ * tb_shard_layout describes one rank's share:
+ *   row_begin, row_end  tile rows [row_begin, row_end) of the height axis,
+ *                       shared out in rank order as evenly as they go, the
+ *                       first ranks one row more (empty past the row count)
+ *   out_row_begin       first output row the rank writes
+ *   out_rows            output rows it writes (sum of its rows' kept extents)
+ *   halo_rows           rows of the band it receives: e_y(row_begin), or 0
+ *                       when it needs none (first rank, empty share, or no
+ *                       blend between the two rows)
+ *   halo_elems          elements of that band (every frame tile and width
+ *                       tile of row row_begin - 1, every plane): the size of
+ *                       the message it receives
+ *   send_elems          elements of the band it sends to rank + 1, or 0
+ */
+typedef struct {
+    int32_t row_begin;
+    int32_t row_end;
+    int64_t out_row_begin;
+    int64_t out_rows;
+    int32_t halo_rows;
+    int64_t halo_elems;
+    int64_t send_elems;
+} tb_shard_layout;
+
+/*
+ * tb_stitch_shard_layout -- rank `rank`'s share of a row-sharded stitch of
+ * the grid (at, ay, ax) (at NULL for a 2D grid) with B x C planes (host only,
+ * no GPU).
+ * Errors: TB_ERR_NULL (ay, ax or out NULL), TB_ERR_SHAPE (negative sizes,
+ * world < 1, rank outside [0, world)), TB_ERR_GEOMETRY, TB_ERR_UNSUPPORTED
+ * (as tb_axis_layout).
+ */
+tb_status tb_stitch_shard_layout(const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int64_t B, int64_t C,
+                                 int32_t world, int32_t rank, tb_shard_layout* out);
+
+/*
+ * tb_stitch_halo_pack -- the band a rank sends to its successor: the last
+ * e_y(row + 1) rows (raw, as decoded) of every tile of tile row `row`, packed
+ * into one dense device buffer, tile by tile in row-major (k, j) order,
+ * each [B, C, L_t(k), e_y(row + 1), L_x(j)] (L_t = 1 for a 2D grid).
+ *
+ *   tiles   host array of the device pointers of tile row `row`: n_x tiles
+ *           (2D, at NULL), or n_t * n_x tiles row-major over (k, j) (3D)
+ *   row     0 .. n_y - 2
+ *   halo    device buffer of send_elems elements of `dtype` (see
+ *           tb_shard_layout); must not overlap a tile
+ * Nothing is launched when e_y(row + 1) is 0.
+ * Errors: TB_ERR_NULL, TB_ERR_DTYPE, TB_ERR_SHAPE (row out of range,
+ * negative sizes), TB_ERR_GEOMETRY, TB_ERR_UNSUPPORTED (more than 512 tiles
+ * in the row), TB_ERR_CUDA.
+ */
+tb_status tb_stitch_halo_pack(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C, const tb_axis* at,
+                              const tb_axis* ay, const tb_axis* ax, int32_t row, void* halo, void* stream);
+
+/*
+ * tb_stitch2d_shard -- rows [row_begin, row_end) of the tile grid stitched
+ * as tb_stitch2d would stitch them in the whole grid: the output rows
+ * [out_row_begin, out_row_begin + out_rows) of the full image, written to
+ * `out` ([B, C, out_rows, out_w]).
+ *
+ *   tiles     host array of (row_end - row_begin) * n_x device pointers,
+ *             row-major; tile (i, j) of the grid is entry
+ *             (i - row_begin) * n_x + j
+ *   halo      device pointer to the band tb_stitch_halo_pack made of row
+ *             row_begin - 1, received from the rank before; required when
+ *             row_begin > 0 and e_y(row_begin) > 0, else ignored
+ *   out_rows  the sum of the kept extents of rows [row_begin, row_end)
+ * Errors as tb_stitch2d, plus TB_ERR_SHAPE for a row range outside
+ * [0, n_y] or out_rows that does not match it.
+ */
+tb_status tb_stitch2d_shard(const void* const* tiles, const void* halo, tb_dtype dtype, int64_t B, int64_t C,
+                            const tb_axis* ay, const tb_axis* ax, int32_t row_begin, int32_t row_end, void* out,
+                            int64_t out_rows, int64_t out_w, void* stream);
+
+/*
+ * tb_stitch3d_shard -- as tb_stitch2d_shard for a video grid, sharded along
+ * the height: tiles holds n_t * (row_end - row_begin) * n_x pointers,
+ * row-major over (k, i - row_begin, j); `halo` the 3D band of row
+ * row_begin - 1; `out` is [B, C, out_t, out_rows, out_w].
+ */
+tb_status tb_stitch3d_shard(const void* const* tiles, const void* halo, tb_dtype dtype, int64_t B, int64_t C,
+                            const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int32_t row_begin,
+                            int32_t row_end, void* out, int64_t out_t, int64_t out_rows, int64_t out_w,
+                            void* stream);
+
+/*
  * One axis of a normalised-ramp tile layout [STU]: n_tiles tiles of one
  * extent, placed by the caller (a planner spreads them so the first starts at
  * 0 and the last ends at out_extent).
@@ -273,19 +371,46 @@ tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dtype dtyp
  *   patches   host array of P device pointers (as tb_patch_gn_stats)
  *   outs      host array of P device pointers, same shapes; outs[p] may
  *             equal patches[p] (in place), other overlaps are not allowed
- *   partials  device array written by tb_patch_gn_stats with the same
- *             arguments on a GPU of the same kind (P * N * G * TB_GN_PARTS
- *             entries; only the records that call filled are read, which
- *             both calls derive from the arguments and the SM count)
+ *   partials  device array of P * N * G * TB_GN_PARTS records written by
+ *             tb_patch_gn_stats for these patches (by one call over all P,
+ *             or by several calls whose record sets lie back to back in
+ *             patch order); every record is read and those with count 0
+ *             are skipped
  *   gamma     device [C] of dtype, or NULL for 1
  *   beta      device [C] of dtype, or NULL for 0
  *   eps       added to the variance (> 0 recommended; >= 0 required)
  *   silu      nonzero applies SiLU
+ * Equivalent to tb_patch_gn_apply_gathered with R = P.
  * Errors as tb_patch_gn_stats, plus TB_ERR_SHAPE for eps < 0 or NaN.
  */
 tb_status tb_patch_gn_apply(const void* const* patches, void* const* outs, int32_t P, tb_dtype dtype, int64_t N,
                             int64_t C, const int64_t* spatial, int32_t G, const tb_gn_partial* partials,
                             const void* gamma, const void* beta, float eps, int32_t silu, void* stream);
+
+/*
+ * tb_patch_gn_apply_gathered -- the apply step of a sharded PatchGroupNorm
+ * [DVA]: each rank holds only its own patch(es), has run tb_patch_gn_stats
+ * on them, and has gathered every rank's records (one all-gather of
+ * N * G * TB_GN_PARTS records per patch, in place of the page's two
+ * all-reduces per norm).  This call pools the statistics of all R record
+ * sets and normalises the P local patches with them.
+ *
+ *   patches, outs, P, dtype, N, C, spatial, G, gamma, beta, eps, silu
+ *             as tb_patch_gn_apply, describing only the local patches
+ *   partials  device array of R record sets of [N][G][TB_GN_PARTS] records,
+ *             back to back: the records of every patch of the whole tensor
+ *             (the local ones included), in any order
+ *   R         record sets in `partials` (>= 1; the total patch count)
+ * The pooled mean and variance are those of every element described by the
+ * records; the call cannot check that they describe the same tensor as the
+ * local patches.
+ * Errors as tb_patch_gn_apply, plus TB_ERR_SHAPE for R < 1 and
+ * TB_ERR_UNSUPPORTED for R > 65536 or R * N * G * TB_GN_PARTS above 2e9.
+ */
+tb_status tb_patch_gn_apply_gathered(const void* const* patches, void* const* outs, int32_t P, tb_dtype dtype,
+                                     int64_t N, int64_t C, const int64_t* spatial, int32_t G,
+                                     const tb_gn_partial* partials, int32_t R, const void* gamma, const void* beta,
+                                     float eps, int32_t silu, void* stream);
 
 /* Most patches (ranks) one Patchify split or patch gather handles. */
 #define TB_MAX_PATCHES 64
@@ -377,7 +502,10 @@ tb_status tb_gather_patches(const void* const* patches, int32_t P, const int64_t
  *     TB_ERR_UNSUPPORTED and launches nothing.
  *   - The first call on each device looks up the scratch array's device
  *     address (cudaGetSymbolAddress, with that device current); make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The address belongs to the
+ *     device's CUDA context: after cudaDeviceReset (or any other teardown of
+ *     the context) the next call finds a new context id and looks the
+ *     address up again, so that call, too, must come before any capture.
  *   - Every call uses the same scratch array.  Each call writes every record
  *     it reads before reading it, so nothing needs clearing, but two calls
  *     whose work overlaps on the GPU (different streams, or different host

@@ -1,6 +1,6 @@
 """Build libtileblend.so for GB300 (sm_103a) with nvcc, in-tree.
 
-Three translation units are compiled in parallel and linked into
+The translation units are compiled in parallel and linked into
 ``patch_groupnorm_gb300/_build/libtileblend.so`` (static CUDA runtime, only
 the C ABI of ``include/tileblend.h`` exported).  The stitch unit is built
 with ``-fmad=false`` so that no multiply and add fuse: the stitch's rounding
@@ -28,6 +28,7 @@ UNITS = {
     "tb_noalloc.cu": [],
     "tb_ramp.cu": [],
     "tb_patchify.cu": [],
+    "tb_shard.cu": [],
 }
 HEADERS = ["tb_internal.h"]
 

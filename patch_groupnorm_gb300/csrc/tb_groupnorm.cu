@@ -19,9 +19,11 @@
 //     mean = meanA + d * nB / n,  M2 = M2A + M2B + d^2 * nA * nB / n.
 //
 // gn_stats_kernel: each (patch, sample, group) unit's elements are cut into
-// `parts` contiguous parts (1, 2, 4 or 8: about two CTAs per SM in all), one
-// CTA per part, and every part's statistics go to their own record (the
-// apply step merges them).  Each thread streams 16-byte chunks through a
+// `parts` contiguous parts (1 .. TB_GN_PARTS, chosen on the host from the
+// sizes and the SM count), one CTA per part; every part's statistics go to
+// their own record and the unit's remaining records get count 0, so the
+// records describe themselves (the apply step merges every record with
+// elements, whatever split produced it).  Each thread streams 16-byte chunks through a
 // ring of cp.async slots, seven ahead.  For fp16 / bf16 it sums x - K and
 // (x - K)^2 over groups of 8 chunks (64 elements) on packed fp32 pairs, K
 // being the group's first element -- differences and squares of 16-bit
@@ -40,8 +42,9 @@
 // griddepcontrol.wait before touching global memory.
 //
 // gn_apply_kernel: one CTA per segment of one channel row.  The CTA issues
-// its data loads, then each warp combines the P * TB_GN_PARTS records of the
-// row's group (pooled_stats) into a = rstd * gamma[c] and
+// its data loads, then each warp combines the R * TB_GN_PARTS records of the
+// row's group (pooled_stats; R record sets, one per patch of the whole
+// tensor, possibly gathered from other ranks) into a = rstd * gamma[c] and
 // b = beta[c] - mean * a; the elements become
 // y = silu(x * a + b), rounded once into the storage type.
 #include <cuda_bf16.h>
@@ -332,7 +335,8 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
     }
 
     // warp, then CTA (fixed order); the part's record, and the empty records
-    // of parts no CTA takes (records rank + j * parts, j >= 1)
+    // of parts no CTA takes (records rank + j * parts, j >= 1: together the
+    // CTAs of a unit write all TB_GN_PARTS of its records)
     acc = warp_reduce(acc);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) s_warp[warp] = acc;
@@ -360,54 +364,63 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
 }
 
 // Pooled (mean, rstd) of group g of sample n from the part records, computed
-// by one warp.  The statistics kernel filled the first `parts` records of
-// every (patch, sample, group) and left the rest empty, so only those are
-// read.  Each record (count c, mean m, M2) adds
-// c, c * (m - K) and M2 + c * (m - K)^2 to three sums taken about K, the mean
-// of the first record with elements (so the sums do not cancel); then
+// by one warp.  `partials` holds R record sets of [N][G][TB_GN_PARTS] (the
+// sets of one or more statistics calls, e.g. gathered from every rank), and
+// every record describes itself: records with count 0 hold no elements and
+// are skipped, whichever call wrote them and however it split its units.
+// Each record (count c, mean m, M2) adds c, c * (m - K) and
+// M2 + c * (m - K)^2 to three sums taken about K, the mean of the first
+// record with elements (so the sums do not cancel); then
 //     mean = K + S1 / n,   M2 = S2 - S1^2 / n   (Chan's combination, summed),
-// and the variance is M2 / n, biased.  Lane 0 holds the result.
+// and the variance is M2 / n, biased.  Counts are summed exactly in 64 bits
+// and converted to fp32 once.  Lane 0 holds the result.
 __device__ __forceinline__ void pooled_stats(const GnApplyParams& p, int64_t n, int64_t g, float& mean, float& rstd) {
     const int lane = threadIdx.x & 31;
-    const int total = p.P * p.parts;  // parts beyond p.parts hold no elements
-    auto record = [&](int q, float& c, float& m, float& m2) {
-        const int pq = q / p.parts, k = q - pq * p.parts;
-        const GnPartial* src = p.partials + (((int64_t)pq * p.N + n) * p.G + g) * TB_GN_PARTS + k;
-        const longlong2 raw = __ldg(reinterpret_cast<const longlong2*>(src));
-        c = (float)raw.x;
+    const int total = p.R * TB_GN_PARTS;
+    const int64_t set_stride = p.N * p.G * TB_GN_PARTS;  // records between consecutive sets
+    const GnPartial* const unit0 = p.partials + (n * p.G + g) * TB_GN_PARTS;
+    auto record = [&](int q, long long& c, float& m, float& m2) {
+        const int r = q / TB_GN_PARTS, k = q - r * TB_GN_PARTS;
+        const longlong2 raw = __ldg(reinterpret_cast<const longlong2*>(unit0 + r * set_stride + k));
+        c = raw.x;
         m = __int_as_float((int)(raw.y & 0xffffffffLL));
         m2 = __int_as_float((int)(raw.y >> 32));
     };
-    // the first 32 records stay in registers (all of them when P <= 4)
-    float c0 = 0.f, m0 = 0.f, v0 = 0.f;
+    // the first 32 records stay in registers (all of them when R <= 4)
+    long long c0 = 0;
+    float m0 = 0.f, v0 = 0.f;
     if (lane < total) record(lane, c0, m0, v0);
     float K = 0.f;
-    unsigned has = __ballot_sync(0xffffffffu, c0 > 0.f);
+    unsigned has = __ballot_sync(0xffffffffu, c0 > 0);
     if (has != 0u) {
         K = __shfl_sync(0xffffffffu, m0, __ffs(has) - 1);
     } else {
         for (int base = 32; base < total; base += 32) {
-            float c = 0.f, m = 0.f, m2 = 0.f;
+            long long c = 0;
+            float m = 0.f, m2 = 0.f;
             if (base + lane < total) record(base + lane, c, m, m2);
-            has = __ballot_sync(0xffffffffu, c > 0.f);
+            has = __ballot_sync(0xffffffffu, c > 0);
             if (has != 0u) {
                 K = __shfl_sync(0xffffffffu, m, __ffs(has) - 1);
                 break;
             }
         }
     }
-    float sn = 0.f, s1 = 0.f, s2 = 0.f;
-    auto add = [&](float c, float m, float m2) {
-        if (c > 0.f) {
+    long long sn = 0;
+    float s1 = 0.f, s2 = 0.f;
+    auto add = [&](long long c, float m, float m2) {
+        if (c > 0) {
+            const float cf = (float)c;
             const float d = m - K;
             sn += c;
-            s1 = fmaf(c, d, s1);
-            s2 += fmaf(c * d, d, m2);
+            s1 = fmaf(cf, d, s1);
+            s2 += fmaf(cf * d, d, m2);
         }
     };
     add(c0, m0, v0);
     for (int q = lane + 32; q < total; q += 32) {
-        float c, m, m2;
+        long long c;
+        float m, m2;
         record(q, c, m, m2);
         add(c, m, m2);
     }
@@ -417,8 +430,9 @@ __device__ __forceinline__ void pooled_stats(const GnApplyParams& p, int64_t n, 
         s1 += __shfl_down_sync(0xffffffffu, s1, delta);
         s2 += __shfl_down_sync(0xffffffffu, s2, delta);
     }
-    const float q1 = sn > 0.f ? s1 / sn : 0.f;
-    const float var = sn > 0.f ? fmaxf(0.f, fmaf(-s1, q1, s2) / sn) : 0.f;  // biased: divide by the count
+    const float nf = (float)sn;
+    const float q1 = sn > 0 ? s1 / nf : 0.f;
+    const float var = sn > 0 ? fmaxf(0.f, fmaf(-s1, q1, s2) / nf) : 0.f;  // biased: divide by the count
     mean = K + q1;
     rstd = 1.0f / sqrtf(var + p.eps);
 }

@@ -255,11 +255,48 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     return TB_OK;
 }
 
+// Rows [row_begin, row_end) of the height axis, stitched by one rank of a
+// row-sharded stitch; `halo` holds the packed band of row row_begin - 1.
+struct Shard {
+    int32_t row_begin, row_end;
+    const void* halo;
+};
+
+// The local height axis of a shard: its tile rows, preceded (when its first
+// row blends with the row above) by a halo row of extent e_y(row_begin) that
+// holds exactly the rows of the row above that the band reads, keeps nothing
+// and blends with nothing.  With that extent the kernel's neighbour row
+// L(n-1) - e(n) + c is band row c, and the plane pitch is the band's.
+bool shard_axis(const Axis& g, int32_t row_begin, int32_t row_end, Axis& l, bool* halo) {
+    if (row_begin < 0 || row_end < row_begin || row_end > g.n) return false;
+    *halo = row_begin > 0 && row_end > row_begin && g.blend[row_begin] > 0;
+    l = Axis{};
+    l.stride = g.stride;
+    l.blend_extent = g.blend_extent;
+    l.row_limit = g.row_limit;
+    int n = 0;
+    if (*halo) {
+        l.ext[n] = g.blend[row_begin];
+        l.blend[n] = 0;
+        l.kept[n] = 0;
+        ++n;
+    }
+    for (int i = row_begin; i < row_end; ++i, ++n) {
+        l.ext[n] = g.ext[i];
+        l.blend[n] = (n == 0) ? 0 : g.blend[i];
+        l.kept[n] = g.kept[i];
+        l.out += g.kept[i];
+    }
+    l.n = n;
+    return true;
+}
+
 tb_status stitch_common(int ndim, const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
                         const tb_axis* at, const tb_axis* ay, const tb_axis* ax, void* out, int64_t out_t,
-                        int64_t out_h, int64_t out_w, void* stream) {
+                        int64_t out_h, int64_t out_w, void* stream, const Shard* shard = nullptr) {
     if (dtype != TB_F32 && dtype != TB_F16 && dtype != TB_BF16) return TB_ERR_DTYPE;
     if (B < 0 || C < 0 || out_t < 0 || out_h < 0 || out_w < 0) return TB_ERR_SHAPE;
+    if (B > 0 && C > INT64_MAX / B) return TB_ERR_SHAPE;
     Axis g[3];
     int64_t ntot = 0;
     if (ndim == 3) {
@@ -276,17 +313,43 @@ tb_status stitch_common(int ndim, const void* const* tiles, tb_dtype dtype, int6
     if (s != TB_OK) return s;
     s = derive_axis(ax, g[2], &ntot);
     if (s != TB_OK) return s;
+    for (int a = 0; a < 3; ++a)
+        if (!bands_apart(g[a])) return TB_ERR_UNSUPPORTED;
+    // a shard stitches its own tile rows, with the band of the row above as
+    // a halo row that is read but not written
+    bool halo = false;
+    const void* table[TB_MAX_TILES];
+    if (shard != nullptr) {
+        Axis l;
+        if (!shard_axis(g[1], shard->row_begin, shard->row_end, l, &halo)) return TB_ERR_SHAPE;
+        const int32_t rows_in = shard->row_end - shard->row_begin;
+        if ((int64_t)g[0].n * (rows_in + (halo ? 1 : 0)) * g[2].n > TB_MAX_TILES) return TB_ERR_UNSUPPORTED;
+        if (halo && shard->halo == nullptr && B * C > 0) return TB_ERR_NULL;
+        if (tiles == nullptr && rows_in > 0 && B * C > 0) return TB_ERR_NULL;
+        const int eb = elem_bytes(dtype);
+        const char* hp = reinterpret_cast<const char*>(shard->halo);
+        int q = 0;
+        for (int k = 0; k < g[0].n; ++k) {
+            if (halo)
+                for (int j = 0; j < g[2].n; ++j) {
+                    table[q++] = hp;
+                    hp += B * C * (int64_t)g[0].ext[k] * l.ext[0] * g[2].ext[j] * eb;
+                }
+            for (int i = 0; i < rows_in; ++i)
+                for (int j = 0; j < g[2].n; ++j) table[q++] = tiles[((int64_t)k * rows_in + i) * g[2].n + j];
+        }
+        g[1] = l;
+        tiles = table;
+    }
     if ((ndim == 3 && out_t != g[0].out) || out_h != g[1].out || out_w != g[2].out) return TB_ERR_SHAPE;
     const int64_t planes = B * C;
     const int64_t ntiles = (int64_t)g[0].n * g[1].n * g[2].n;
-    if (planes == 0 || ntiles == 0) return TB_OK;  // nothing to write
+    if (planes == 0 || ntiles == 0 || g[1].out == 0) return TB_OK;  // nothing to write
     if (B > 0 && planes / B != C) return TB_ERR_SHAPE;
     if (tiles == nullptr || out == nullptr) return TB_ERR_NULL;
     if (ntiles > TB_MAX_TILES) return TB_ERR_UNSUPPORTED;
     for (int64_t q = 0; q < ntiles; ++q)
         if (tiles[q] == nullptr) return TB_ERR_NULL;
-    for (int a = 0; a < 3; ++a)
-        if (!bands_apart(g[a])) return TB_ERR_UNSUPPORTED;
     // every tile's element count must fit the kernel's 64-bit offsets (always)
     // and the output row count its 32-bit row arithmetic (checked at launch)
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -324,12 +387,12 @@ tb_status gn_validate(const void* const* patches, int32_t P, tb_dtype dtype, int
     return TB_OK;
 }
 
-// CTAs per GroupNorm statistics unit, which is also the number of records
-// per (patch, sample, group) the statistics kernel fills: 1, 2, 4 or 8
-// (dividing TB_GN_PARTS), about two CTAs per SM in all, each streaming
-// >= 16 KB.  Measured on GB300: more, shorter CTAs per unit lose more to
-// their fixed costs than they gain.  Both GroupNorm calls derive it from the
-// same arguments, so the apply step reads exactly the records filled.
+// CTAs per GroupNorm statistics unit (each writes one of the unit's
+// TB_GN_PARTS records; the rest get count 0): 1, 2, 4 or 8, about two CTAs
+// per SM in all, each streaming >= 16 KB.  Measured on GB300: more, shorter
+// CTAs per unit lose more to their fixed costs than they gain.  Only the
+// statistics call uses it: the records describe themselves, so the apply
+// step reads every record and needs no agreement with this choice.
 tb_status gn_parts(int32_t P, int64_t N, int64_t C, const int64_t* spatial, int32_t G, tb_dtype dtype, int* parts) {
     int64_t max_len = 0;
     for (int p = 0; p < P; ++p) max_len = std::max(max_len, (C / G) * spatial[p]);
@@ -344,6 +407,57 @@ tb_status gn_parts(int32_t P, int64_t N, int64_t C, const int64_t* spatial, int3
     while (k * 2 <= TB_GN_PARTS && k * 2 <= want) k *= 2;
     if (TB_GN_FORCE_PARTS > 0) k = TB_GN_FORCE_PARTS;
     *parts = k;
+    return TB_OK;
+}
+
+// The apply step over R record sets (R = P for the plain two-call path).
+tb_status gn_apply(const void* const* patches, void* const* outs, int32_t P, tb_dtype dtype, int64_t N, int64_t C,
+                   const int64_t* spatial, int32_t G, const tb_gn_partial* partials, int32_t R, const void* gamma,
+                   const void* beta, float eps, int32_t silu, void* stream) {
+    tb_status s = gn_validate(patches, P, dtype, N, C, spatial, G, partials);
+    if (s != TB_OK) return s;
+    if (R < 1) return TB_ERR_SHAPE;
+    if ((double)R * (double)N * (double)G * TB_GN_PARTS > 2.0e9 || R > 65536) return TB_ERR_UNSUPPORTED;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return TB_ERR_SHAPE;
+    if (outs == nullptr) return TB_ERR_NULL;
+    if (N == 0 || C == 0) return TB_OK;
+    for (int p = 0; p < P; ++p)
+        if (spatial[p] > 0 && outs[p] == nullptr) return TB_ERR_NULL;
+    tb::GnApplyParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    const int vec = 16 / elem_bytes(dtype);
+    bool aligned = true;
+    for (int p = 0; p < P; ++p) {
+        if (spatial[p] > 0 && (spatial[p] % vec != 0 || !aligned16(patches[p]) || !aligned16(outs[p])))
+            aligned = false;
+    }
+    const int64_t seg = tb::gn_apply_segment((int)dtype, aligned);
+    int64_t items = 0;
+    for (int p = 0; p < P; ++p) {
+        prm.patches[p] = patches[p];
+        prm.outs[p] = outs[p];
+        prm.spatial[p] = spatial[p];
+        prm.item_start[p] = items;
+        prm.nseg[p] = spatial[p] > 0 ? (spatial[p] + seg - 1) / seg : 1;
+        if (spatial[p] > 0) items += N * C * prm.nseg[p];
+    }
+    prm.item_start[P] = items;  // a patch with no elements owns an empty item range
+    if (items == 0) return TB_OK;
+    if (items > 2147483647LL) return TB_ERR_UNSUPPORTED;
+    prm.partials = reinterpret_cast<const tb::GnPartial*>(partials);
+    prm.gamma = gamma;
+    prm.beta = beta;
+    prm.N = N;
+    prm.C = C;
+    prm.P = P;
+    prm.G = G;
+    prm.seg = (int32_t)seg;
+    prm.R = R;
+    prm.eps = eps;
+    prm.silu = silu ? 1 : 0;
+    prm.aligned = aligned ? 1 : 0;
+    cudaError_t e = tb::launch_gn_apply(prm, (int)dtype, items, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
     return TB_OK;
 }
 
@@ -518,7 +632,7 @@ tb_status ramp_axis(const tb_ramp_axis* a, int gran, tb::RampAxisK& k) {
 // C ABI
 // ===========================================================================
 
-TB_API size_t tb_version(void) { return 10000 * 0 + 100 * 2 + 0; }
+TB_API size_t tb_version(void) { return 10000 * 0 + 100 * 3 + 0; }
 
 TB_API const char* tb_status_string(tb_status s) {
     switch (s) {
@@ -567,6 +681,133 @@ TB_API tb_status tb_stitch3d(const void* const* tiles, tb_dtype dtype, int64_t B
                              int64_t out_w, void* stream) {
     if (at == nullptr) return TB_ERR_NULL;
     return stitch_common(3, tiles, dtype, B, C, at, ay, ax, out, out_t, out_h, out_w, stream);
+}
+
+// The three axes of a 2D (at == NULL) or 3D grid, validated.
+tb_status grid_axes(const tb_axis* at, const tb_axis* ay, const tb_axis* ax, Axis (&g)[3]) {
+    int64_t ntot = 0;
+    if (at != nullptr) {
+        tb_status s = derive_axis(at, g[0], &ntot);
+        if (s != TB_OK) return s;
+    } else {
+        g[0].n = 1;
+        g[0].ext[0] = 1;
+        g[0].kept[0] = 1;
+        g[0].blend[0] = 0;
+        g[0].out = 1;
+    }
+    tb_status s = derive_axis(ay, g[1], &ntot);
+    if (s != TB_OK) return s;
+    return derive_axis(ax, g[2], &ntot);
+}
+
+// Elements of the packed band of tile row `row`'s last e rows (all frame
+// tiles, all width tiles, all planes).
+int64_t band_elems(const Axis (&g)[3], int64_t planes, int32_t e) {
+    int64_t frames = 0, width = 0;
+    for (int k = 0; k < g[0].n; ++k) frames += g[0].ext[k];
+    for (int j = 0; j < g[2].n; ++j) width += g[2].ext[j];
+    return planes * frames * (int64_t)e * width;
+}
+
+TB_API tb_status tb_stitch_shard_layout(const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int64_t B, int64_t C,
+                                        int32_t world, int32_t rank, tb_shard_layout* out) {
+    if (ay == nullptr || ax == nullptr || out == nullptr) return TB_ERR_NULL;
+    if (B < 0 || C < 0 || world < 1 || rank < 0 || rank >= world) return TB_ERR_SHAPE;
+    if (B > 0 && C > INT64_MAX / B) return TB_ERR_SHAPE;
+    Axis g[3];
+    tb_status s = grid_axes(at, ay, ax, g);
+    if (s != TB_OK) return s;
+    // tile rows shared out in rank order, the first ranks one row more
+    const int32_t n = g[1].n, each = n / world, extra = n % world;
+    const int32_t begin = rank * each + std::min(rank, extra);
+    const int32_t end = begin + each + (rank < extra ? 1 : 0);
+    tb_shard_layout l{};
+    l.row_begin = begin;
+    l.row_end = end;
+    for (int i = 0; i < begin; ++i) l.out_row_begin += g[1].kept[i];
+    for (int i = begin; i < end; ++i) l.out_rows += g[1].kept[i];
+    const int64_t planes = B * C;
+    if (end > begin && begin > 0 && g[1].blend[begin] > 0) {
+        l.halo_rows = g[1].blend[begin];
+        l.halo_elems = band_elems(g, planes, l.halo_rows);
+    }
+    if (end > begin && end < n && g[1].blend[end] > 0) l.send_elems = band_elems(g, planes, g[1].blend[end]);
+    *out = l;
+    return TB_OK;
+}
+
+TB_API tb_status tb_stitch_halo_pack(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
+                                     const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int32_t row, void* halo,
+                                     void* stream) {
+    if (dtype != TB_F32 && dtype != TB_F16 && dtype != TB_BF16) return TB_ERR_DTYPE;
+    if (ay == nullptr || ax == nullptr) return TB_ERR_NULL;
+    if (B < 0 || C < 0) return TB_ERR_SHAPE;
+    if (B > 0 && C > INT64_MAX / B) return TB_ERR_SHAPE;
+    Axis g[3];
+    tb_status s = grid_axes(at, ay, ax, g);
+    if (s != TB_OK) return s;
+    if (row < 0 || row + 1 >= g[1].n) return TB_ERR_SHAPE;
+    const int32_t e = g[1].blend[row + 1];
+    const int64_t planes = B * C;
+    if (e == 0 || planes == 0) return TB_OK;
+    const int64_t ntiles = (int64_t)g[0].n * g[2].n;
+    if (ntiles > tb::HALO_MAXT) return TB_ERR_UNSUPPORTED;
+    if (tiles == nullptr || halo == nullptr) return TB_ERR_NULL;
+    for (int64_t q = 0; q < ntiles; ++q)
+        if (tiles[q] == nullptr) return TB_ERR_NULL;
+    const int eb = elem_bytes(dtype);
+    // widest chunk dividing every row, band offset and address
+    int vb = 16;
+    auto fit = [&vb](uint64_t v) {
+        while (vb > 1 && v % (uint64_t)vb != 0) vb >>= 1;
+    };
+    fit((uint64_t)reinterpret_cast<uintptr_t>(halo));
+    for (int j = 0; j < g[2].n; ++j) fit((uint64_t)g[2].ext[j] * eb);
+    for (int64_t q = 0; q < ntiles; ++q) fit((uint64_t)reinterpret_cast<uintptr_t>(tiles[q]));
+    tb::HaloPackParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.dst = halo;
+    prm.e = e;
+    prm.ntiles = (int32_t)ntiles;
+    const int64_t ly = g[1].ext[row];
+    int64_t off = 0, most = 0;
+    for (int k = 0; k < g[0].n; ++k)
+        for (int j = 0; j < g[2].n; ++j) {
+            const int64_t q = (int64_t)k * g[2].n + j;
+            const int64_t w = (int64_t)g[2].ext[j] * eb / vb;
+            if (w > 2147483647LL || planes * g[0].ext[k] * ly * w > (INT64_MAX >> 1)) return TB_ERR_UNSUPPORTED;
+            prm.src[q] = tiles[q];
+            prm.rows[q] = (int32_t)ly;
+            prm.width[q] = (int32_t)w;
+            prm.n[q] = planes * g[0].ext[k] * e * w;
+            prm.dst_off[q] = off;
+            off += prm.n[q];
+            most = std::max(most, prm.n[q]);
+        }
+    const int64_t cta = 16384 / vb;  // 16 KB per CTA
+    prm.per_cta = cta;
+    const int64_t ranges = (most + cta - 1) / cta;
+    if (ranges > 2147483647LL) return TB_ERR_UNSUPPORTED;
+    cudaError_t e2 = tb::launch_halo_pack(prm, vb, ranges, reinterpret_cast<cudaStream_t>(stream));
+    if (e2 != cudaSuccess) return cuda_fail(e2);
+    return TB_OK;
+}
+
+TB_API tb_status tb_stitch2d_shard(const void* const* tiles, const void* halo, tb_dtype dtype, int64_t B, int64_t C,
+                                   const tb_axis* ay, const tb_axis* ax, int32_t row_begin, int32_t row_end,
+                                   void* out, int64_t out_rows, int64_t out_w, void* stream) {
+    const Shard sh{row_begin, row_end, halo};
+    return stitch_common(2, tiles, dtype, B, C, nullptr, ay, ax, out, 1, out_rows, out_w, stream, &sh);
+}
+
+TB_API tb_status tb_stitch3d_shard(const void* const* tiles, const void* halo, tb_dtype dtype, int64_t B, int64_t C,
+                                   const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int32_t row_begin,
+                                   int32_t row_end, void* out, int64_t out_t, int64_t out_rows, int64_t out_w,
+                                   void* stream) {
+    if (at == nullptr) return TB_ERR_NULL;
+    const Shard sh{row_begin, row_end, halo};
+    return stitch_common(3, tiles, dtype, B, C, at, ay, ax, out, out_t, out_rows, out_w, stream, &sh);
 }
 
 TB_API tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
@@ -682,52 +923,14 @@ TB_API tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dty
 TB_API tb_status tb_patch_gn_apply(const void* const* patches, void* const* outs, int32_t P, tb_dtype dtype, int64_t N,
                                    int64_t C, const int64_t* spatial, int32_t G, const tb_gn_partial* partials,
                                    const void* gamma, const void* beta, float eps, int32_t silu, void* stream) {
-    tb_status s = gn_validate(patches, P, dtype, N, C, spatial, G, partials);
-    if (s != TB_OK) return s;
-    if (!(eps >= 0.0f) || std::isinf(eps)) return TB_ERR_SHAPE;
-    if (outs == nullptr) return TB_ERR_NULL;
-    if (N == 0 || C == 0) return TB_OK;
-    for (int p = 0; p < P; ++p)
-        if (spatial[p] > 0 && outs[p] == nullptr) return TB_ERR_NULL;
-    tb::GnApplyParams prm;
-    std::memset(&prm, 0, sizeof(prm));
-    const int vec = 16 / elem_bytes(dtype);
-    bool aligned = true;
-    for (int p = 0; p < P; ++p) {
-        if (spatial[p] > 0 && (spatial[p] % vec != 0 || !aligned16(patches[p]) || !aligned16(outs[p])))
-            aligned = false;
-    }
-    const int64_t seg = tb::gn_apply_segment((int)dtype, aligned);
-    int64_t items = 0;
-    for (int p = 0; p < P; ++p) {
-        prm.patches[p] = patches[p];
-        prm.outs[p] = outs[p];
-        prm.spatial[p] = spatial[p];
-        prm.item_start[p] = items;
-        prm.nseg[p] = spatial[p] > 0 ? (spatial[p] + seg - 1) / seg : 1;
-        if (spatial[p] > 0) items += N * C * prm.nseg[p];
-    }
-    prm.item_start[P] = items;  // a patch with no elements owns an empty item range
-    if (items == 0) return TB_OK;
-    if (items > 2147483647LL) return TB_ERR_UNSUPPORTED;
-    prm.partials = reinterpret_cast<const tb::GnPartial*>(partials);
-    prm.gamma = gamma;
-    prm.beta = beta;
-    prm.N = N;
-    prm.C = C;
-    prm.P = P;
-    prm.G = G;
-    prm.seg = (int32_t)seg;
-    int parts = 1;
-    s = gn_parts(P, N, C, spatial, G, dtype, &parts);
-    if (s != TB_OK) return s;
-    prm.parts = parts;
-    prm.eps = eps;
-    prm.silu = silu ? 1 : 0;
-    prm.aligned = aligned ? 1 : 0;
-    cudaError_t e = tb::launch_gn_apply(prm, (int)dtype, items, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e);
-    return TB_OK;
+    return gn_apply(patches, outs, P, dtype, N, C, spatial, G, partials, P, gamma, beta, eps, silu, stream);
+}
+
+TB_API tb_status tb_patch_gn_apply_gathered(const void* const* patches, void* const* outs, int32_t P, tb_dtype dtype,
+                                            int64_t N, int64_t C, const int64_t* spatial, int32_t G,
+                                            const tb_gn_partial* partials, int32_t R, const void* gamma,
+                                            const void* beta, float eps, int32_t silu, void* stream) {
+    return gn_apply(patches, outs, P, dtype, N, C, spatial, G, partials, R, gamma, beta, eps, silu, stream);
 }
 
 TB_API tb_status tb_patchify_layout(int64_t extent, int32_t factor, int32_t P, int64_t* starts, int64_t* sizes) {

@@ -213,6 +213,31 @@ static_assert(sizeof(PatchCopyParams) <= 32000, "kernel parameter block too larg
 cudaError_t launch_patch_copy(const PatchCopyParams& p, int vec, bool to_patches, int64_t grid, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
+// Row-sharded stitch: packing the band a rank sends to its successor
+// ---------------------------------------------------------------------------
+
+constexpr int HALO_MAXT = 512;      // tiles in one tile row (all frame tiles x width tiles)
+constexpr int HALO_BLOCK = 256;
+
+// Band q is the last `e` rows of every frame of every plane of source tile
+// q, packed densely: [planes][frames_q][e][width_q] chunks at chunk dst_off[q]
+// of the halo buffer.  Offsets and sizes are in chunks of the launch's width.
+struct HaloPackParams {
+    const void* src[HALO_MAXT];
+    int64_t dst_off[HALO_MAXT];
+    int64_t n[HALO_MAXT];          // chunks of band q
+    int32_t rows[HALO_MAXT];       // rows per frame of source tile q
+    int32_t width[HALO_MAXT];      // chunks per row of source tile q
+    void* dst;
+    int64_t per_cta;               // chunks one CTA copies
+    int32_t e;                     // band rows
+    int32_t ntiles;
+};
+static_assert(sizeof(HaloPackParams) <= 32000, "kernel parameter block too large");
+
+cudaError_t launch_halo_pack(const HaloPackParams& p, int vec_bytes, int64_t ranges, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // PatchGroupNorm
 // ---------------------------------------------------------------------------
 
@@ -231,10 +256,10 @@ static_assert(TB_GN_PARTS >= 1 && TB_GN_PARTS <= 32 && (TB_GN_PARTS & (TB_GN_PAR
 struct GnStatsParams {
     const void* patches[GN_MAXP];
     int64_t spatial[GN_MAXP];     // elements per channel in patch p
-    GnPartial* partials;          // [P][N][G]
+    GnPartial* partials;          // [P][N][G][TB_GN_PARTS]
     int64_t N, C;
     int32_t P, G;
-    int32_t parts;                // CTAs per (p, n, g) unit: 1, 2, 4 or 8 (divides TB_GN_PARTS)
+    int32_t parts;                // CTAs per (p, n, g) unit: 1 .. TB_GN_PARTS
     int32_t aligned;              // every unit start and length is a multiple of the vector width
 };
 
@@ -250,7 +275,7 @@ struct GnApplyParams {
     int64_t N, C;
     int32_t P, G;
     int32_t seg;                      // elements per segment
-    int32_t parts;                    // records per (p, n, g) the statistics kernel filled
+    int32_t R;                        // record sets in `partials`: [R][N][G][TB_GN_PARTS]
     float eps;
     int32_t silu;
     int32_t aligned;                  // every channel row start is 16-byte aligned

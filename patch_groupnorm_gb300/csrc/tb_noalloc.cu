@@ -9,10 +9,12 @@
 //
 // The array holds TB_NOALLOC_MAX_PARTIALS 16-byte records (1 MiB) on every
 // device that loads the library, for the life of the process: the
-// TB_GN_PARTS records of each of up to 8192 (patch, sample, group) units.  Calls share
-// it: each call's statistics kernel writes every record its apply kernel
-// reads, so nothing needs clearing between calls, but calls whose work
-// overlaps on the GPU race on it.
+// TB_GN_PARTS records of each of up to 8192 (patch, sample, group) units.
+// Calls share it: each call's statistics kernel writes every record its
+// apply kernel reads, so nothing needs clearing between calls, but calls
+// whose work overlaps on the GPU race on it.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "tb_internal.h"
@@ -25,12 +27,54 @@ namespace {
 static __device__ __align__(256) tb::GnPartial g_noalloc_partials[TB_NOALLOC_MAX_PARTIALS];
 
 constexpr int MAX_DEVICES = 64;
-std::mutex g_addr_mu;
-void* g_addr[MAX_DEVICES] = {};
 
-// Device address of the scratch array on the current device.  Host code sees
-// the array's name only as a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// The scratch array's device address, as looked up in one CUDA context.  A
+// device reset destroys the context and the library's module with it; the
+// module loaded into the next context may place the array elsewhere.  So
+// the cached address is tied to the process-unique id of the context it was
+// looked up in, and a call in any other context looks it up again.
+struct ScratchAddr {
+    unsigned long long ctx_id;
+    void* addr;
+};
+std::mutex g_addr_mu;
+ScratchAddr g_addr[MAX_DEVICES] = {};
+
+// Driver calls reached through the runtime's entry-point query, so that the
+// library links no driver library and still loads on machines without one.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+bool g_driver_looked_up = false;
+
+// Id of the calling thread's current context, or 0 if there is none yet (the
+// runtime binds it lazily) or the driver calls are unavailable.
+unsigned long long current_context_id() {
+    if (!g_driver_looked_up) {
+        g_driver_looked_up = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+    }
+    if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id + 1;  // 0 stays "unknown"
+}
+
+// Device address of the scratch array in the current context.  Host code
+// sees the array's name only as a host-side stand-in, so the address comes
+// from cudaGetSymbolAddress, looked up once per device (and again after the
+// device's context has been replaced), with that device current.
 tb_status scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -40,16 +84,19 @@ tb_status scratch_address(void** out) {
     }
     if (dev < 0 || dev >= MAX_DEVICES) return TB_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_addr_mu);
-    if (g_addr[dev] == nullptr) {
+    const unsigned long long id = current_context_id();
+    ScratchAddr& c = g_addr[dev];
+    if (c.addr == nullptr || id == 0 || id != c.ctx_id) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_partials);
         if (e != cudaSuccess || p == nullptr) {
             tb::record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
             return TB_ERR_CUDA;
         }
-        g_addr[dev] = p;
+        c.addr = p;
+        c.ctx_id = current_context_id();  // bound now, if it was not before
     }
-    *out = g_addr[dev];
+    *out = c.addr;
     return TB_OK;
 }
 

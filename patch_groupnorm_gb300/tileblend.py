@@ -55,6 +55,12 @@ class tb_gn_partial(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("mean", ctypes.c_float), ("m2", ctypes.c_float)]
 
 
+class tb_shard_layout(ctypes.Structure):
+    _fields_ = [("row_begin", ctypes.c_int32), ("row_end", ctypes.c_int32), ("out_row_begin", ctypes.c_int64),
+                ("out_rows", ctypes.c_int64), ("halo_rows", ctypes.c_int32), ("halo_elems", ctypes.c_int64),
+                ("send_elems", ctypes.c_int64)]
+
+
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
 _P_vp = ctypes.POINTER(ctypes.c_void_p)
 _P_i32 = ctypes.POINTER(ctypes.c_int32)
@@ -79,6 +85,21 @@ _lib.tb_patch_gn_apply.restype = ctypes.c_int
 _lib.tb_patch_gn_apply.argtypes = [_P_vp, _P_vp, _i32, ctypes.c_int, _i64, _i64, _P_i64, _i32, _vp, _vp, _vp,
                                    ctypes.c_float, _i32, _vp]
 
+_lib.tb_patch_gn_apply_gathered.restype = ctypes.c_int
+_lib.tb_patch_gn_apply_gathered.argtypes = [_P_vp, _P_vp, _i32, ctypes.c_int, _i64, _i64, _P_i64, _i32, _vp, _i32,
+                                            _vp, _vp, ctypes.c_float, _i32, _vp]
+_lib.tb_stitch_shard_layout.restype = ctypes.c_int
+_lib.tb_stitch_shard_layout.argtypes = [_P_axis, _P_axis, _P_axis, _i64, _i64, _i32, _i32,
+                                        ctypes.POINTER(tb_shard_layout)]
+_lib.tb_stitch_halo_pack.restype = ctypes.c_int
+_lib.tb_stitch_halo_pack.argtypes = [_P_vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _P_axis, _i32, _vp, _vp]
+_lib.tb_stitch2d_shard.restype = ctypes.c_int
+_lib.tb_stitch2d_shard.argtypes = [_P_vp, _vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _i32, _i32, _vp, _i64,
+                                   _i64, _vp]
+_lib.tb_stitch3d_shard.restype = ctypes.c_int
+_lib.tb_stitch3d_shard.argtypes = [_P_vp, _vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _P_axis, _i32, _i32, _vp,
+                                   _i64, _i64, _i64, _vp]
+
 _lib.tb_stitch2d_ramp.restype = ctypes.c_int
 _lib.tb_stitch2d_ramp.argtypes = [_P_vp, ctypes.c_int, _i64, _i64, ctypes.POINTER(tb_ramp_axis),
                                   ctypes.POINTER(tb_ramp_axis), _vp, _vp]
@@ -95,8 +116,10 @@ _lib.tb_gather_patches.argtypes = [_P_vp, _i32, _P_i64, ctypes.c_int, _i32, _P_i
 TB_MAX_PATCHES = 64
 
 EXPORTED = ("tb_version", "tb_status_string", "tb_last_cuda_error", "tb_axis_layout", "tb_stitch2d",
-            "tb_stitch3d", "tb_stitch2d_ramp", "tb_patch_gn_stats", "tb_patch_gn_apply",
-            "tb_patch_group_norm_noalloc", "tb_patchify_layout", "tb_patchify", "tb_gather_patches")
+            "tb_stitch3d", "tb_stitch_shard_layout", "tb_stitch_halo_pack", "tb_stitch2d_shard",
+            "tb_stitch3d_shard", "tb_stitch2d_ramp", "tb_patch_gn_stats", "tb_patch_gn_apply",
+            "tb_patch_gn_apply_gathered", "tb_patch_group_norm_noalloc", "tb_patchify_layout", "tb_patchify",
+            "tb_gather_patches")
 
 
 class TileBlendError(RuntimeError):
@@ -257,6 +280,111 @@ def tb_stitch2d_raw(tile_ptrs: Sequence[int], dtype: int, B: int, C: int, ay: Ax
 
 
 # ---------------------------------------------------------------------------
+# row-sharded stitch
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class ShardLayout:
+    row_begin: int
+    row_end: int
+    out_row_begin: int
+    out_rows: int
+    halo_rows: int
+    halo_elems: int
+    send_elems: int
+
+
+def _axis_ref(a: Optional[Axis]):
+    if a is None:
+        return None, None
+    c = a.c()
+    return c, ctypes.byref(c)
+
+
+def tb_stitch_shard_layout(at: Optional[Axis], ay: Axis, ax: Axis, B: int, C: int, world: int,
+                           rank: int) -> ShardLayout:
+    """Rank ``rank``'s share of a stitch whose tile rows are split over
+    ``world`` ranks (host only)."""
+    _, pt = _axis_ref(at)
+    _, py = _axis_ref(ay)
+    _, px = _axis_ref(ax)
+    out = tb_shard_layout()
+    _check(_lib.tb_stitch_shard_layout(pt, py, px, B, C, world, rank, ctypes.byref(out)), "tb_stitch_shard_layout")
+    return ShardLayout(out.row_begin, out.row_end, out.out_row_begin, out.out_rows, out.halo_rows, out.halo_elems,
+                       out.send_elems)
+
+
+def _flat_tiles(tiles, ndim: int) -> List[torch.Tensor]:
+    if ndim == 2:
+        return [t for row in tiles for t in row]
+    return [t for plane in tiles for row in plane for t in row]
+
+
+def tb_stitch_halo_pack(row_tiles, at: Optional[Axis], ay: Axis, ax: Axis, row: int, halo: torch.Tensor,
+                        stream=None) -> torch.Tensor:
+    """Pack the last e_y(row + 1) rows of every tile of tile row ``row`` into
+    ``halo`` (1D, ``send_elems`` elements).  ``row_tiles`` is the list of the
+    row's tiles: ``[t_j]`` for a 2D grid, ``[[t_kj]]`` (frame tile major) for
+    a 3D grid."""
+    flat = list(row_tiles) if at is None else [t for per_k in row_tiles for t in per_k]
+    for q, t in enumerate(flat):
+        _cuda_contig(t, "tile %d" % q)
+    _cuda_contig(halo, "halo")
+    B, C = flat[0].shape[:2]
+    _, pt = _axis_ref(at)
+    _, py = _axis_ref(ay)
+    _, px = _axis_ref(ax)
+    _check(_lib.tb_stitch_halo_pack(_ptr_array([t.data_ptr() for t in flat]), _dtype_code(halo), B, C, pt, py, px,
+                                    row, halo.data_ptr(), _stream_handle(stream)), "tb_stitch_halo_pack")
+    return halo
+
+
+def tb_stitch2d_shard(tiles, halo: Optional[torch.Tensor], ay: Axis, ax: Axis, row_begin: int, row_end: int,
+                      out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Stitch tile rows [row_begin, row_end) (``tiles[i - row_begin][j]``)
+    with the band ``halo`` of the row above into ``out`` ([B, C, out_rows,
+    W])."""
+    _cuda_contig(out, "out")
+    B, C, H, W = out.shape
+    flat = _flat_tiles(tiles, 2)
+    for q, t in enumerate(flat):
+        _cuda_contig(t, "tile %d" % q)
+        if t.dtype != out.dtype:
+            raise ValueError("tile %d has dtype %s, out %s" % (q, t.dtype, out.dtype))
+    hp = None
+    if halo is not None:
+        _cuda_contig(halo, "halo")
+        hp = halo.data_ptr()
+    a_y, a_x = ay.c(), ax.c()
+    _check(_lib.tb_stitch2d_shard(_ptr_array([t.data_ptr() for t in flat]), hp, _dtype_code(out), B, C,
+                                  ctypes.byref(a_y), ctypes.byref(a_x), row_begin, row_end, out.data_ptr(), H, W,
+                                  _stream_handle(stream)), "tb_stitch2d_shard")
+    return out
+
+
+def tb_stitch3d_shard(tiles, halo: Optional[torch.Tensor], at: Axis, ay: Axis, ax: Axis, row_begin: int,
+                      row_end: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """3D form of ``tb_stitch2d_shard``: ``tiles[k][i - row_begin][j]``,
+    ``out`` [B, C, T, out_rows, W]."""
+    _cuda_contig(out, "out")
+    B, C, T, H, W = out.shape
+    flat = _flat_tiles(tiles, 3)
+    for q, t in enumerate(flat):
+        _cuda_contig(t, "tile %d" % q)
+        if t.dtype != out.dtype:
+            raise ValueError("tile %d has dtype %s, out %s" % (q, t.dtype, out.dtype))
+    hp = None
+    if halo is not None:
+        _cuda_contig(halo, "halo")
+        hp = halo.data_ptr()
+    a_t, a_y, a_x = at.c(), ay.c(), ax.c()
+    _check(_lib.tb_stitch3d_shard(_ptr_array([t.data_ptr() for t in flat]), hp, _dtype_code(out), B, C,
+                                  ctypes.byref(a_t), ctypes.byref(a_y), ctypes.byref(a_x), row_begin, row_end,
+                                  out.data_ptr(), T, H, W, _stream_handle(stream)), "tb_stitch3d_shard")
+    return out
+
+
+# ---------------------------------------------------------------------------
 # normalised-ramp stitch
 # ---------------------------------------------------------------------------
 
@@ -383,6 +511,39 @@ def tb_patch_gn_apply(patches: Sequence[torch.Tensor], outs: Sequence[torch.Tens
                                   gamma.data_ptr() if gamma is not None else None,
                                   beta.data_ptr() if beta is not None else None, float(eps), 1 if silu else 0,
                                   _stream_handle(stream)), "tb_patch_gn_apply")
+    return outs
+
+
+def tb_patch_gn_apply_gathered(patches: Sequence[torch.Tensor], outs: Sequence[torch.Tensor], G: int,
+                               partials: torch.Tensor, R: int, gamma: Optional[torch.Tensor],
+                               beta: Optional[torch.Tensor], eps: float, silu: bool = True,
+                               stream=None) -> Sequence[torch.Tensor]:
+    """Normalise the local ``patches`` with the pooled statistics of ``R``
+    record sets (``partials``: [R, N, G, TB_GN_PARTS, 2] int64, e.g. every
+    rank's records after an all-gather)."""
+    N, C, dt, spatial, ptrs = _gn_args(patches)
+    P = len(patches)
+    if len(outs) != P:
+        raise ValueError("one output per patch")
+    optrs = []
+    for q, (o, t) in enumerate(zip(outs, patches)):
+        _cuda_contig(o, "out %d" % q)
+        if o.shape != t.shape or o.dtype != t.dtype:
+            raise ValueError("out %d must match patch %d" % (q, q))
+        optrs.append(o.data_ptr())
+    for name, v in (("gamma", gamma), ("beta", beta)):
+        if v is not None:
+            _cuda_contig(v, name)
+            if v.numel() != C or v.dtype != patches[0].dtype:
+                raise ValueError("%s must be [C] of the patches' dtype" % name)
+    _cuda_contig(partials, "partials")
+    if partials.numel() * partials.element_size() != R * N * G * TB_GN_PARTS * 16:
+        raise ValueError("partials must hold R*N*G*TB_GN_PARTS 16-byte records")
+    sp = (ctypes.c_int64 * P)(*spatial)
+    _check(_lib.tb_patch_gn_apply_gathered(_ptr_array(ptrs), _ptr_array(optrs), P, dt, N, C, sp, G,
+                                           partials.data_ptr(), R, gamma.data_ptr() if gamma is not None else None,
+                                           beta.data_ptr() if beta is not None else None, float(eps),
+                                           1 if silu else 0, _stream_handle(stream)), "tb_patch_gn_apply_gathered")
     return outs
 
 

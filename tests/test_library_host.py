@@ -279,3 +279,88 @@ def test_product_path_and_oracle_share_no_code():
         assert "tileblend" not in open(path).read(), path
     for path in glob.glob(os.path.join(ROOT, "patch_groupnorm_gb300", "csrc", "*")):
         assert "oracle" not in open(path).read().lower(), path
+
+
+# --------------------------------------------------------------------------
+# row-sharded stitch layout and the gathered GroupNorm apply (host side)
+# --------------------------------------------------------------------------
+
+def _expected_shares(lay, world, planes, frames, width):
+    """Tile rows dealt in rank order (the first ranks one more), each rank's
+    output rows, and the bands crossing each rank boundary, recomputed from
+    the oracle's geometry."""
+    n = lay.n
+    out = []
+    begin = 0
+    for r in range(world):
+        rows = n // world + (1 if r < n % world else 0)
+        end = begin + rows
+        halo = lay.blends[begin] if (rows and begin > 0) else 0
+        send = lay.blends[end] if (rows and end < n) else 0
+        out.append((begin, end, sum(lay.kept[:begin]), sum(lay.kept[begin:end]), halo,
+                    planes * frames * halo * width, planes * frames * send * width))
+        begin = end
+    return out
+
+
+@pytest.mark.parametrize("case", [
+    (None, (256, 64, 0.25, 8), (256, 64, 0.25, 8), 4, 3),
+    (None, (200, 120, 0.25, 8), (256, 72, 0.25, 8), 1, 3),
+    ((49, 16, 0.25, 1), (60, 32, 0.25, 8), (104, 32, 0.25, 8), 1, 3),
+    (None, (30, 8, 0.0, 8), (20, 8, 0.0, 4), 2, 2),
+])
+def test_shard_layout_matches_the_oracle_geometry(tbl, case):
+    at, ay, ax, B, C = case
+    lt = axis_layout(*at) if at else None
+    ly, lx = axis_layout(*ay), axis_layout(*ax)
+    frames = sum(lt.extents) if lt else 1
+    for world in (1, 2, 3, ly.n, ly.n + 3):
+        want = _expected_shares(ly, world, B * C, frames, sum(lx.extents))
+        for r in range(world):
+            got = tbl.tb_stitch_shard_layout(tbl.Axis(*at) if at else None, tbl.Axis(*ay), tbl.Axis(*ax), B, C,
+                                             world, r)
+            assert (got.row_begin, got.row_end, got.out_row_begin, got.out_rows, got.halo_rows, got.halo_elems,
+                    got.send_elems) == want[r], (world, r)
+        # the shares tile the output rows exactly
+        assert sum(w[3] for w in want) == ly.out_extent
+
+
+def test_shard_calls_reject_before_launch(tbl):
+    ay, ax = tbl.Axis(256, 64, 0.25, 8), tbl.Axis(128, 64, 0.25, 8)
+    a_y, a_x = ay.c(), ax.c()
+    out = tbl.tb_shard_layout()
+    f = tbl._lib.tb_stitch_shard_layout
+    assert f(None, ctypes.byref(a_y), ctypes.byref(a_x), 1, 3, 0, 0, ctypes.byref(out)) == tbl.TB_ERR_SHAPE
+    assert f(None, ctypes.byref(a_y), ctypes.byref(a_x), 1, 3, 2, 2, ctypes.byref(out)) == tbl.TB_ERR_SHAPE
+    assert f(None, None, ctypes.byref(a_x), 1, 3, 2, 0, ctypes.byref(out)) == tbl.TB_ERR_NULL
+    pack = tbl._lib.tb_stitch_halo_pack
+    arr = (ctypes.c_void_p * 3)(16, 32, 48)
+    # the last tile row lends no band; a row past the grid is refused
+    assert pack(arr, 2, 1, 3, None, ctypes.byref(a_y), ctypes.byref(a_x), 5, 16, None) == tbl.TB_ERR_SHAPE
+    assert pack(arr, 2, 1, 3, None, ctypes.byref(a_y), ctypes.byref(a_x), -1, 16, None) == tbl.TB_ERR_SHAPE
+    assert pack(arr, 2, 1, 3, None, ctypes.byref(a_y), ctypes.byref(a_x), 0, None, None) == tbl.TB_ERR_NULL
+    assert pack(arr, 9, 1, 3, None, ctypes.byref(a_y), ctypes.byref(a_x), 0, 16, None) == tbl.TB_ERR_DTYPE
+    st = tbl._lib.tb_stitch2d_shard
+    tiles = (ctypes.c_void_p * 9)(*([16] * 9))
+    # rows 3..6 need the band of row 2
+    assert st(tiles, None, 2, 1, 3, ctypes.byref(a_y), ctypes.byref(a_x), 3, 6, 16, 896, 1024, None) \
+        == tbl.TB_ERR_NULL
+    assert st(tiles, 16, 2, 1, 3, ctypes.byref(a_y), ctypes.byref(a_x), 3, 6, 16, 895, 1024, None) \
+        == tbl.TB_ERR_SHAPE
+    assert st(tiles, 16, 2, 1, 3, ctypes.byref(a_y), ctypes.byref(a_x), 4, 3, 16, 0, 1024, None) \
+        == tbl.TB_ERR_SHAPE
+    assert st(tiles, 16, 2, 1, 3, ctypes.byref(a_y), ctypes.byref(a_x), 0, 7, 16, 0, 1024, None) \
+        == tbl.TB_ERR_SHAPE
+    # an empty share writes nothing
+    assert st(None, None, 2, 1, 3, ctypes.byref(a_y), ctypes.byref(a_x), 6, 6, None, 0, 1024, None) == tbl.TB_OK
+
+
+def test_gathered_apply_rejects_before_launch(tbl):
+    ptrs = (ctypes.c_void_p * 1)(16)
+    sp = (ctypes.c_int64 * 1)(100)
+    g = tbl._lib.tb_patch_gn_apply_gathered
+    eps = ctypes.c_float(1e-6)
+    assert g(ptrs, ptrs, 1, 2, 1, 64, sp, 32, 16, 0, None, None, eps, 1, None) == tbl.TB_ERR_SHAPE      # R < 1
+    assert g(ptrs, ptrs, 1, 2, 1, 64, sp, 32, 16, 65537, None, None, eps, 1, None) == tbl.TB_ERR_UNSUPPORTED
+    assert g(ptrs, ptrs, 1, 2, 1, 64, sp, 32, None, 4, None, None, eps, 1, None) == tbl.TB_ERR_NULL
+    assert g(ptrs, ptrs, 1, 2, 1, 60, sp, 32, 16, 4, None, None, eps, 1, None) == tbl.TB_ERR_SHAPE     # C % G
