@@ -20,6 +20,7 @@ The JSON line also carries:
               source (null if the source changed since);
   kernels     every kernel on its own workload: rotating buffer sets (no
               L2 reuse), launches replayed from a CUDA graph, CUDA events;
+              and one launch at a time after an L2 flush (us_single);
   cpu_baseline  the CPU oracle timed on this host: whole steps for about 10 s
               on all cores (one plane per thread) and 10 s single-threaded.
 
@@ -397,15 +398,41 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def per_kernel(torch, tb, W, dev, peak, reps):
-    """Every kernel on its own workload.  Enough input/output sets rotate that
-    no launch finds its data in L2 (> 3x the 129 MB L2 between reuses); the
-    launches are captured in a CUDA graph and replayed, so host call overhead
-    is excluded; per-launch time = replay time / launches (median of reps)."""
+def per_kernel(torch, tb, W, dev, peak, reps, only=None):
+    """Every kernel on its own workload, timed two ways.
+
+    replay: enough input/output sets rotate that no launch finds its data in
+    L2 (> 3x the 129 MB L2 between reuses); the launches are captured in a
+    CUDA graph and replayed back to back, so host call overhead is excluded;
+    per-launch time = replay time / launches (median of reps).
+    single: one launch at a time, cold: before each, a 258 MB fill evicts L2
+    and the GPU then spins for about 2 ms, long enough for the host to queue
+    the start event, the launch and the end event behind it, so the events
+    bracket the launch alone and no host time is timed; median of reps.
+    This is the figure comparable with ncu's serialised gpu__time_duration."""
     stream = torch.cuda.Stream(dev)
     res = []
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def single_ms(launch_set, nsets):
+        ts = []
+        with torch.cuda.stream(stream):
+            for r in range(reps + 2):
+                flush.fill_(float(r))
+                torch.cuda._sleep(4_000_000)     # ~2 ms at 2 GHz: the host queues what follows
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                launch_set(r % nsets)
+                b.record(stream)
+                b.synchronize()
+                if r >= 2:
+                    ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
 
     def timed(launch_set, nsets, nbytes, name, workload, per_graph=60):
+        if only and workload not in only and name not in only:
+            return
         with torch.cuda.stream(stream):
             for q in range(nsets):          # warm-up, outside capture
                 launch_set(q)
@@ -427,14 +454,23 @@ def per_kernel(torch, tb, W, dev, peak, reps):
                 ts.append(a.elapsed_time(b) / per_graph)
         ms = statistics.median(ts)
         gbs = nbytes / (ms * 1e-3) / 1e9
-        res.append({"kernel": name, "workload": workload, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
-                    "frac_of_peak": round(gbs / peak, 4), "bytes": nbytes, "sets": nsets})
         del g
+        ms1 = single_ms(launch_set, nsets)
+        gbs1 = nbytes / (ms1 * 1e-3) / 1e9
+        res.append({"kernel": name, "workload": workload, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                    "frac_of_peak": round(gbs / peak, 4), "us_single": round(ms1 * 1e3, 2),
+                    "GB/s_single": round(gbs1, 1), "frac_single": round(gbs1 / peak, 4), "bytes": nbytes,
+                    "sets": nsets})
 
     def nsets_for(nbytes):
         return max(2, math.ceil(3 * L2_BYTES / nbytes) + 1)
 
+    def wanted(name, *kernels):
+        return not only or name in only or any(k in only for k in kernels)
+
     for name, w in W.STITCH.items():
+        if not wanted(name, "stitch2d", "stitch3d"):
+            continue
         axes = [tb.Axis(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in w.axes]
         lays = [tb.tb_axis_layout(a) for a in axes]
         tiles = W.make_stitch_tiles(w, [list(zip(l.origins, l.extents)) for l in lays], [l.out_extent for l in lays])
@@ -455,6 +491,8 @@ def per_kernel(torch, tb, W, dev, peak, reps):
         del sets
         torch.cuda.empty_cache()
     for name, w in W.RAMP.items():
+        if not wanted(name, "stitch2d_ramp"):
+            continue
         ay = tb.RampAxis.spread(w.latent_hw[0], w.latent_tile, w.n_tiles[0], w.scale)
         ax = tb.RampAxis.spread(w.latent_hw[1], w.latent_tile, w.n_tiles[1], w.scale)
         tiles = W.make_ramp_tiles(w, ay, ax)
@@ -469,6 +507,8 @@ def per_kernel(torch, tb, W, dev, peak, reps):
         del sets
         torch.cuda.empty_cache()
     for name, w in W.GROUPNORM.items():
+        if not wanted(name, "gn_stats", "gn_apply"):
+            continue
         patches, gamma, beta = W.make_groupnorm_inputs(w)
         elems = sum(p.numel() for p in patches)
         es = patches[0].element_size()
@@ -484,6 +524,8 @@ def per_kernel(torch, tb, W, dev, peak, reps):
         del sets
         torch.cuda.empty_cache()
     for name, w in W.PATCHIFY.items():
+        if not wanted(name, "patchify", "gather_patches"):
+            continue
         x = W.make_patchify_input(w)
         nbytes = 2 * x.numel() * x.element_size()     # every element read once and written once
         _, sizes = tb.tb_patchify_layout(w.shape[w.axis], w.factor, w.ranks)
@@ -500,6 +542,22 @@ def per_kernel(torch, tb, W, dev, peak, reps):
         del sets
         torch.cuda.empty_cache()
     return res
+
+
+def run_kernels_only(args):
+    """Per-kernel timings of the named workloads or kernels, one JSON line."""
+    import torch
+    from patch_groupnorm_gb300 import build as lib_build
+    if not os.environ.get("TILEBLEND_LIB"):
+        lib_build.build()
+    from patch_groupnorm_gb300 import tileblend as tb
+    from patch_groupnorm_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, _ = measured_peaks()
+    only = set(args.kernels_only.split(","))
+    res = per_kernel(torch, tb, W, dev, peak, args.kernel_reps, only=only)
+    print(json.dumps({"lib": tb.LIB_PATH, "kernels": res}), flush=True)
 
 
 def run_profile_target(args):
@@ -680,6 +738,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kernels", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--kernels-only", default=None,
+                    help="comma-separated workloads or kernel names: print only their per-kernel timings")
     ap.add_argument("--profile", default=None,
                     help="KERNEL:WORKLOAD (stitch2d|stitch3d|gn_stats|gn_apply): plain launches for ncu")
     args = ap.parse_args()
@@ -687,6 +747,9 @@ def main():
         args.warmup = 3
     if args.profile:
         run_profile_target(args)
+        return
+    if args.kernels_only:
+        run_kernels_only(args)
         return
     if args.impl == "reference":
         if "--steps" not in sys.argv:

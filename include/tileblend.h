@@ -412,6 +412,22 @@ tb_status tb_patch_gn_apply_gathered(const void* const* patches, void* const* ou
                                      const tb_gn_partial* partials, int32_t R, const void* gamma, const void* beta,
                                      float eps, int32_t silu, void* stream);
 
+/*
+ * tb_device_status -- the library's device-side status word on the current
+ * device.  Kernels never trap: a kernel that cannot complete a piece of work
+ * (a wait for its tensor copies that exceeds about one second; in a build
+ * with bounds checks, an index outside its tile or output) records a code
+ * and skips that work.  The first code recorded stays until cleared.
+ *   code    out: 0 (TB_DEV_OK) or the first code recorded
+ *   clear   nonzero resets the word to 0 after reading it
+ * Synchronises with the device (a blocking copy from the word).  Errors:
+ * TB_ERR_NULL, TB_ERR_CUDA.
+ */
+#define TB_DEV_OK 0u
+#define TB_DEV_WAIT_TIMEOUT 1u
+#define TB_DEV_OUT_OF_BOUNDS 2u
+tb_status tb_device_status(uint32_t* code, int32_t clear);
+
 /* Most patches (ranks) one Patchify split or patch gather handles. */
 #define TB_MAX_PATCHES 64
 

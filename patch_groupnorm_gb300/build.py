@@ -29,6 +29,7 @@ UNITS = {
     "tb_ramp.cu": [],
     "tb_patchify.cu": [],
     "tb_shard.cu": [],
+    "tb_status.cu": [],
 }
 HEADERS = ["tb_internal.h"]
 
@@ -38,27 +39,39 @@ def _nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def lib_path(variant: str = "") -> str:
+    """Path of the library build `variant` ('' is the product build)."""
+    return LIB if not variant else os.path.join(OUT_DIR, "libtileblend-%s.so" % variant)
+
+
+def _stale(path: str) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(path)
     deps = [os.path.join(CSRC, u) for u in UNITS] + [os.path.join(CSRC, h) for h in HEADERS]
     deps.append(os.path.join(INCLUDE, "tileblend.h"))
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library if it is missing or out of date."""
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, variant: str = "", defines=()) -> str:
+    """Compile and link the library if it is missing or out of date.
+
+    `variant` with `defines` (preprocessor definitions such as
+    "TB_DEBUG_BOUNDS=1") builds a separate library, libtileblend-<variant>.so,
+    next to the product build; the binding loads it when the environment
+    variable TILEBLEND_LIB names it."""
+    path = lib_path(variant)
+    if not force and not _stale(path):
+        return path
     os.makedirs(OUT_DIR, exist_ok=True)
     nvcc = _nvcc()
-    tag = str(os.getpid())
+    tag = "%s%d" % (variant + "." if variant else "", os.getpid())
+    dflags = ["-D" + d for d in defines]
 
     def compile_unit(unit):
         obj = os.path.join(OUT_DIR, unit.rsplit(".", 1)[0] + "." + tag + ".o")
-        cmd = [nvcc, *ARCH, *COMMON, *UNITS[unit], "-c", os.path.join(CSRC, unit), "-o", obj]
+        cmd = [nvcc, *ARCH, *COMMON, *dflags, *UNITS[unit], "-c", os.path.join(CSRC, unit), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -70,15 +83,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(UNITS)) as pool:
         objs = list(pool.map(compile_unit, UNITS))
-    tmp = LIB + "." + tag + ".tmp"
+    tmp = path + "." + tag + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
+    os.replace(tmp, path)
     for o in objs:
         os.remove(o)
-    return LIB
+    return path
 
 
 if __name__ == "__main__":

@@ -19,6 +19,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "tb_internal.h"
 #include "tileblend.h"
@@ -39,6 +40,16 @@
 #endif
 #ifndef TB_RAMP_MAX_ROWS_PER_THREAD
 #define TB_RAMP_MAX_ROWS_PER_THREAD 16
+#endif
+// Stitch path for aligned grids of up to 128 tiles: 1 stages each piece's
+// sources with tensor copies (TMA), 0 always streams them through the
+// per-thread cp.async rings.
+#ifndef TB_STITCH_TMA
+#define TB_STITCH_TMA 1
+#endif
+// Rows of a TMA-path piece for 2-byte types (4-byte types take half).
+#ifndef TB_STITCH_TMA_ROWS
+#define TB_STITCH_TMA_ROWS 32
 #endif
 // CTAs per GroupNorm statistics unit (a power of two dividing TB_GN_PARTS);
 // 0 picks it from the sizes and the SM count.
@@ -150,6 +161,191 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // stitch
 // ---------------------------------------------------------------------------
 
+// ---------------------------------------------------------------------------
+// stitch, TMA path
+// ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, reached through the runtime (no driver
+// library is linked); null if unavailable.
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// Tile shape of the TMA path: `rb` rows per piece (= TMA box rows), TMA box
+// `wbc` chunks wide, pieces at most `wpc` chunks wide, and the shared memory
+// the widest piece's sources take.
+struct TmaShape {
+    int rb = 0, wbc = 0, wpc = 0;
+    int64_t smem = 0;
+};
+
+// Picks the TMA tile shape for the grid's boxes: the cheapest by a rough cost
+// (bytes staged, including rows and columns read past a box's edge, plus a
+// per-copy and a per-CTA charge) among shapes whose pieces fit the shared
+// memory budget.  False if no shape fits.
+bool pick_tma_shape(const Axis (&g)[3], int ndim, int vec, int eb, TmaShape& out) {
+    struct Box {
+        int nodes, nt, ny, w;
+    };
+    Box boxes[4 * 8 * 8];  // distinct box shapes suffice for the cost; cap below
+    int nbx = 0;
+    int64_t weight[4 * 8 * 8];
+    for (int k = 0; k < g[0].n; ++k)
+        for (int i = 0; i < g[1].n; ++i)
+            for (int j = 0; j < g[2].n; ++j) {
+                const int ebt = (ndim == 3 && k > 0) ? std::min(g[0].blend[k], g[0].kept[k]) : 0;
+                const int eby = i > 0 ? std::min(g[1].blend[i], g[1].kept[i]) : 0;
+                const int ebx = j > 0 ? std::min(g[2].blend[j], g[2].kept[j]) : 0;
+                for (int b = (ndim == 3 ? 7 : 3); b >= 0; --b) {
+                    const tb::BoxShape sh = tb::box_shape(b, g[0].kept[k], g[1].kept[i], g[2].kept[j], ebt, eby,
+                                                          ebx, vec);
+                    if (sh.nt <= 0 || sh.ny <= 0 || sh.width <= 0) continue;
+                    const Box bx{1 << ((b & 1) + ((b >> 1) & 1) + ((b >> 2) & 1)), sh.nt, sh.ny, sh.width};
+                    int f = 0;
+                    while (f < nbx && !(boxes[f].nodes == bx.nodes && boxes[f].nt == bx.nt &&
+                                        boxes[f].ny == bx.ny && boxes[f].w == bx.w))
+                        ++f;
+                    if (f == nbx) {
+                        if (nbx == (int)(sizeof(boxes) / sizeof(boxes[0]))) return false;
+                        boxes[nbx] = bx;
+                        weight[nbx] = 0;
+                        ++nbx;
+                    }
+                    ++weight[f];
+                }
+            }
+    const int base_rows = std::max(8, TB_STITCH_TMA_ROWS * 2 / eb);
+    const int rows_c[] = {base_rows, base_rows / 2, base_rows * 3 / 4, base_rows * 5 / 4, base_rows * 3 / 2};
+    const int max_wbc = 256 * eb / 16;  // a TMA box is at most 256 elements wide
+    bool found = false;
+    double best = 0.0;
+    for (int rb : rows_c) {
+        if (rb < 8 || rb % 8 != 0 || rb > 256) continue;
+        for (int wbc = std::max(1, 64 / 16); wbc <= max_wbc; ++wbc) {  // boxes of at least 64 bytes per row
+            int maxw = 0;
+            for (int f = 0; f < nbx; ++f) maxw = std::max(maxw, boxes[f].w);
+            // widest piece (a multiple of the box width) whose sources fit
+            int wpc = ((maxw + wbc - 1) / wbc) * wbc;
+            int64_t smem = 0;
+            while (wpc >= wbc) {
+                smem = 0;
+                for (int f = 0; f < nbx; ++f) {
+                    const int wp = std::min(boxes[f].w, wpc);
+                    smem = std::max<int64_t>(smem, (int64_t)boxes[f].nodes * rb * ((wp + wbc - 1) / wbc) * wbc * 16);
+                }
+                if (smem <= tb::TMA_SMEM_BUDGET) break;
+                wpc -= wbc;
+            }
+            if (wpc < wbc) continue;
+            double cost = 0.0;
+            for (int f = 0; f < nbx; ++f) {
+                const Box& bx = boxes[f];
+                const int64_t rblk = (bx.ny + rb - 1) / rb, cblk = (bx.w + wpc - 1) / wpc;
+                const int64_t pieces = (int64_t)bx.nt * rblk * cblk;
+                int64_t copies = 0, staged = 0;
+                for (int64_t c = 0; c < cblk; ++c) {
+                    const int wp = (int)std::min<int64_t>(wpc, bx.w - c * wpc);
+                    const int nb = (wp + wbc - 1) / wbc;
+                    copies += nb;
+                    staged += (int64_t)nb * wbc * 16 * rb;
+                }
+                cost += (double)weight[f] * bx.nt * rblk * bx.nodes * (staged + 512.0 * copies) +
+                        (double)weight[f] * pieces * 8192.0;
+            }
+            if (!found || cost < best) {
+                found = true;
+                best = cost;
+                out.rb = rb;
+                out.wbc = wbc;
+                out.wpc = wpc;
+                out.smem = smem;
+            }
+        }
+    }
+    return found;
+}
+
+// Launches the TMA path for an aligned grid; *launched stays false when the
+// grid does not suit it (then the ring path runs).
+tb_status try_launch_tma(const tb::StitchParamsSmall& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, int vec,
+                         int64_t planes, const void* const* tiles, cudaStream_t stream, bool* launched) {
+    *launched = false;
+    const int ntiles = g[0].n * g[1].n * g[2].n;
+    if (!TB_STITCH_TMA || vec == 1 || ntiles > tb::TMA_MAXT) return TB_OK;
+    if (planes > 2147483647LL) return TB_OK;
+    EncodeTiledFn encode = encode_tiled();
+    if (encode == nullptr) return TB_OK;
+    const int eb = elem_bytes(dtype);
+    TmaShape sh;
+    if (!pick_tma_shape(g, ndim, vec, eb, sh)) return TB_OK;
+    static thread_local tb::StitchTmaParams tp;  // 24 KB: kept off the stack
+    std::memset(&tp, 0, sizeof(tp));
+    tp.g = prm;
+    tp.rb = sh.rb;
+    tp.wb = sh.wbc * vec;
+    tp.wpc = sh.wpc;
+    tp.status = tb::device_status_word();
+    const CUtensorMapDataType dt = dtype == TB_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == TB_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    int max_pieces = 0;
+    for (int k = 0; k < g[0].n; ++k)
+        for (int i = 0; i < g[1].n; ++i)
+            for (int j = 0; j < g[2].n; ++j) {
+                const int q = (k * g[1].n + i) * g[2].n + j;
+                const cuuint64_t dims[4] = {(cuuint64_t)g[2].ext[j], (cuuint64_t)g[1].ext[i],
+                                            (cuuint64_t)g[0].ext[k], (cuuint64_t)planes};
+                const cuuint64_t strides[3] = {(cuuint64_t)g[2].ext[j] * eb, (cuuint64_t)g[1].ext[i] * g[2].ext[j] * eb,
+                                               (cuuint64_t)g[0].ext[k] * g[1].ext[i] * g[2].ext[j] * eb};
+                const cuuint32_t box[4] = {(cuuint32_t)tp.wb, (cuuint32_t)tp.rb, 1, 1};
+                const cuuint32_t estr[4] = {1, 1, 1, 1};
+                if (encode(&tp.maps[q], dt, 4, const_cast<void*>(tiles[q]), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                    return TB_OK;
+                const int ebt = (ndim == 3 && k > 0) ? std::min(g[0].blend[k], g[0].kept[k]) : 0;
+                const int eby = i > 0 ? std::min(g[1].blend[i], g[1].kept[i]) : 0;
+                const int ebx = j > 0 ? std::min(g[2].blend[j], g[2].kept[j]) : 0;
+                max_pieces = std::max(max_pieces, tb::tma_tile_pieces(ndim, g[0].kept[k], g[1].kept[i],
+                                                                      g[2].kept[j], ebt, eby, ebx, vec, sh.rb,
+                                                                      sh.wpc));
+            }
+    if (max_pieces == 0 || max_pieces > 65535 || (int64_t)ntiles * planes > 2147483647LL) return TB_OK;
+    int max_ebx = 0, max_eby = 0, max_ebt = 0;
+    for (int j = 1; j < g[2].n; ++j) max_ebx = std::max(max_ebx, std::min(g[2].blend[j], g[2].kept[j]));
+    for (int i = 1; i < g[1].n; ++i) max_eby = std::max(max_eby, std::min(g[1].blend[i], g[1].kept[i]));
+    for (int k = 1; ndim == 3 && k < g[0].n; ++k) max_ebt = std::max(max_ebt, std::min(g[0].blend[k], g[0].kept[k]));
+    const int64_t coef = (int64_t)(2 * (max_ebx + max_eby + max_ebt)) * 4;
+    tb::StitchLaunch l{};
+    l.ndim = ndim;
+    l.dtype = (int)dtype;
+    l.vec = vec;
+    l.grid_x = (int)(ntiles * planes);
+    l.grid_y = max_pieces;
+    l.grid_z = 1;
+    const int64_t smem = 128 + 128 + ((coef + 127) / 128) * 128 + sh.smem;  // alignment slack, mbarrier
+    if (smem > 200 * 1024) return TB_OK;
+    l.smem = (int)smem;
+    cudaError_t e = tb::launch_stitch_tma(tp, l, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *launched = true;
+    return TB_OK;
+}
+
 template <class P>
 tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, int64_t planes,
                           const void* const* tiles, void* out, cudaStream_t stream, bool large) {
@@ -232,10 +428,10 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     l.grid_x = (int)(ntiles * planes);
     l.grid_y = max_pieces;
     l.grid_z = 1;
-    // vector path: 8 staging slots of 16 bytes per thread, then coefficients
+    // vector path: STITCH_SLOTS staging slots of 16 bytes per thread, then coefficients
     int max_ebt = 0;
     for (int k = 1; ndim == 3 && k < g[0].n; ++k) max_ebt = std::max(max_ebt, std::min(g[0].blend[k], g[0].kept[k]));
-    l.smem = (vec > 1 ? 8 * tb::STITCH_BLOCK * 16 : 0) +
+    l.smem = (vec > 1 ? tb::STITCH_SLOTS * tb::STITCH_BLOCK * 16 : 0) +
              (int)(sizeof(float) * 2 * (size_t)(max_ebx + max_eby + max_ebt));
     // byte pitches of a frame of any tile and of the output fit 32 bits
     for (int i = 0; i < g[1].n; ++i)
@@ -249,6 +445,9 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     if constexpr (sizeof(P) == sizeof(tb::StitchParamsLarge)) {
         e = tb::launch_stitch_large(prm, l, stream);
     } else {
+        bool launched = false;
+        tb_status st = try_launch_tma(prm, g, ndim, dtype, vec, planes, tiles, stream, &launched);
+        if (st != TB_OK || launched) return st;
         e = tb::launch_stitch_small(prm, l, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e);

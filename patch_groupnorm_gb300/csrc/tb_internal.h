@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "tileblend.h"
@@ -49,6 +50,12 @@ using StitchParamsLarge = StitchParams<LARGE_MAXA, LARGE_MAXT, LARGE_MAXC>;
 static_assert(sizeof(StitchParamsLarge) <= 32000, "kernel parameter block too large");
 
 constexpr int STITCH_BLOCK = 256;
+// 16-byte staging slots per thread on the stitch's vector path (rows in
+// flight x source nodes).
+#ifndef TB_STITCH_SLOTS
+#define TB_STITCH_SLOTS 8
+#endif
+constexpr int STITCH_SLOTS = TB_STITCH_SLOTS;
 
 // The kept part of a tile splits into up to 2^d boxes by band membership:
 // box b has bit 2 set if it lies in the tile's time band, bit 1 in its
@@ -145,6 +152,62 @@ struct StitchLaunch {
 // Implemented in tb_stitch.cu.
 cudaError_t launch_stitch_small(const StitchParamsSmall& p, const StitchLaunch& l, cudaStream_t s);
 cudaError_t launch_stitch_large(const StitchParamsLarge& p, const StitchLaunch& l, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Stitch, TMA path: each CTA stages every source rectangle of its piece into
+// shared memory with tensor copies (one mbarrier, one memory latency), then
+// evaluates the same closed form from shared memory.
+// ---------------------------------------------------------------------------
+
+constexpr int TMA_MAXT = 128;            // tiles (one tensor map each)
+constexpr int TMA_SMEM_BUDGET = 64 * 1024;
+
+// A piece of box b (BoxShape s): one frame, `rb` rows, `wpc` chunks of
+// columns.  Pieces are numbered column block fastest, then row block, then
+// frame.
+__host__ __device__ inline int tma_box_pieces(const BoxShape& s, int rb, int wpc) {
+    return s.nt * ((s.ny + rb - 1) / rb) * ((s.width + wpc - 1) / wpc);
+}
+
+__host__ __device__ inline int tma_tile_pieces(int ndim, int Kt, int Ky, int Kx, int ebt, int eby, int ebx, int vec,
+                                               int rb, int wpc) {
+    int total = 0;
+    const int nb = ndim == 3 ? 8 : 4;
+    for (int b = nb - 1; b >= 0; --b) {
+        const BoxShape s = box_shape(b, Kt, Ky, Kx, ebt, eby, ebx, vec);
+        if (s.nt <= 0 || s.ny <= 0 || s.width <= 0) continue;
+        total += tma_box_pieces(s, rb, wpc);
+    }
+    return total;
+}
+
+// Parameters of a TMA-path launch: one tensor map per source tile, viewing
+// it as [planes][L_t][L_y][L_x] with a box of `wb` columns x `rb` rows, and
+// the geometry of the ring path's parameters (their tile pointers unused).
+struct alignas(128) StitchTmaParams {
+    CUtensorMap maps[TMA_MAXT];
+    StitchParamsSmall g;
+    uint32_t* status;    // device status word (may be null)
+    int32_t rb;          // rows per piece (= TMA box rows)
+    int32_t wb;          // TMA box columns (elements)
+    int32_t wpc;         // piece width in 16-byte chunks (a multiple of wb's)
+    int32_t node_bytes;  // shared-memory bytes of one source rectangle
+};
+static_assert(sizeof(StitchTmaParams) <= 32000, "kernel parameter block too large");
+
+cudaError_t launch_stitch_tma(const StitchTmaParams& p, const StitchLaunch& l, cudaStream_t s);
+
+// Device status word: 0, or the first problem a kernel reported.
+enum DeviceStatus : uint32_t { DEV_OK = 0, DEV_WAIT_TIMEOUT = 1, DEV_OUT_OF_BOUNDS = 2 };
+static_assert(DEV_OK == TB_DEV_OK && DEV_WAIT_TIMEOUT == TB_DEV_WAIT_TIMEOUT &&
+                  DEV_OUT_OF_BOUNDS == TB_DEV_OUT_OF_BOUNDS,
+              "status codes differ from the header");
+// Its device address in the current context (null if it cannot be looked up).
+uint32_t* device_status_word();
+// Process-unique id (+1) of the calling thread's current CUDA context; 0 if
+// none is bound yet.  Device addresses of the library's static device arrays
+// are cached per context id: a device reset replaces the context and module.
+unsigned long long current_context_id();
 
 // ---------------------------------------------------------------------------
 // Normalised-ramp stitch

@@ -13,8 +13,6 @@
 // Calls share it: each call's statistics kernel writes every record its
 // apply kernel reads, so nothing needs clearing between calls, but calls
 // whose work overlaps on the GPU race on it.
-#include <cuda.h>
-
 #include <mutex>
 
 #include "tb_internal.h"
@@ -40,37 +38,6 @@ struct ScratchAddr {
 std::mutex g_addr_mu;
 ScratchAddr g_addr[MAX_DEVICES] = {};
 
-// Driver calls reached through the runtime's entry-point query, so that the
-// library links no driver library and still loads on machines without one.
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-CtxGetCurrentFn g_ctx_get_current = nullptr;
-CtxGetIdFn g_ctx_get_id = nullptr;
-bool g_driver_looked_up = false;
-
-// Id of the calling thread's current context, or 0 if there is none yet (the
-// runtime binds it lazily) or the driver calls are unavailable.
-unsigned long long current_context_id() {
-    if (!g_driver_looked_up) {
-        g_driver_looked_up = true;
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
-        f = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
-    }
-    if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return 0;
-    CUcontext ctx = nullptr;
-    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
-    unsigned long long id = 0;
-    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
-    return id + 1;  // 0 stays "unknown"
-}
-
 // Device address of the scratch array in the current context.  Host code
 // sees the array's name only as a host-side stand-in, so the address comes
 // from cudaGetSymbolAddress, looked up once per device (and again after the
@@ -84,7 +51,7 @@ tb_status scratch_address(void** out) {
     }
     if (dev < 0 || dev >= MAX_DEVICES) return TB_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_addr_mu);
-    const unsigned long long id = current_context_id();
+    const unsigned long long id = tb::current_context_id();
     ScratchAddr& c = g_addr[dev];
     if (c.addr == nullptr || id == 0 || id != c.ctx_id) {
         void* p = nullptr;
@@ -94,7 +61,7 @@ tb_status scratch_address(void** out) {
             return TB_ERR_CUDA;
         }
         c.addr = p;
-        c.ctx_id = current_context_id();  // bound now, if it was not before
+        c.ctx_id = tb::current_context_id();  // bound now, if it was not before
     }
     *out = c.addr;
     return TB_OK;

@@ -419,8 +419,6 @@ __device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p,
 // 16-byte path: a per-thread cp.async pipeline through shared memory
 // ---------------------------------------------------------------------------
 
-// Staging slots per thread (16 bytes each): rows in flight x source nodes.
-constexpr int STITCH_SLOTS = 8;
 
 __host__ __device__ constexpr int nodes_of(int need) { return 1 << popc3(need); }
 __host__ __device__ constexpr int stages_of(int need) {
@@ -704,6 +702,262 @@ __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_
 #undef TB_BOX_ARGS
 }
 
+// ---------------------------------------------------------------------------
+// TMA path: a CTA stages every source rectangle of its piece with tensor
+// copies that complete on one mbarrier, so the piece costs one memory latency
+// however many rows it has; the closed form is then evaluated from shared
+// memory exactly as on the ring path.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+// One box [wb columns, rb rows] of a [planes][L_t][L_y][L_x] tile at
+// (x, y, t, plane) into shared memory; completes `bar`'s transaction count.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int t, int plane,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(t), "r"(plane), "r"(bar)
+        : "memory");
+}
+
+// A piece waits for its copies at most this long (nanoseconds of the
+// global timer), then reports DEV_WAIT_TIMEOUT and gives up.
+#ifndef TB_TMA_WAIT_NS
+#define TB_TMA_WAIT_NS 1000000000ull
+#endif
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+struct TmaPiece {
+    int64_t plane;
+    int k, i, j;      // tile
+    int t, y, x;      // tile-local frame, first row, first column (elements)
+    int rows, wc;     // valid rows, width in chunks
+};
+
+template <int NDIM, int NEED, int DT>
+__device__ __forceinline__ void run_box_tma(const StitchTmaParams& tp, const TmaPiece& pc, const float* s_xw,
+                                            const float* s_xu, const float* s_yw, const float* s_yu,
+                                            const float* s_tw, const float* s_tu, uint32_t bar, uint32_t s_data) {
+    constexpr int VEC = 16 / Elt<DT>::BYTES;
+    constexpr int NN = NDIM == 3 ? 8 : 4;
+    constexpr int NU = nodes_of(NEED);
+    using C = Chunk<DT, VEC>;
+    const auto& p = tp.g;
+    const auto& AT = p.ax[0];
+    const auto& AY = p.ax[1];
+    const auto& AX = p.ax[2];
+    const int cpb = tp.wb / VEC;                          // chunks per TMA box row
+    const int nblk = (pc.wc + cpb - 1) / cpb;             // TMA boxes per source row block
+    const uint32_t box_bytes = (uint32_t)tp.rb * (uint32_t)tp.wb * Elt<DT>::BYTES;
+    const uint32_t node_bytes = (uint32_t)nblk * box_bytes;
+
+    // warp 0 arms the barrier and issues every copy: node n, box bk
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) mbar_expect_tx(bar, (uint32_t)NU * node_bytes);
+        __syncwarp();
+        for (int q = threadIdx.x; q < NU * nblk; q += 32) {
+            const int n = q / nblk, bk = q - n * nblk;
+            int m = 0;  // the n-th subset of NEED in increasing order
+#pragma unroll
+            for (int mm = 0, r = 0; mm < NN; ++mm)
+                if ((mm & ~NEED) == 0) {
+                    if (r == n) m = mm;
+                    ++r;
+                }
+            const int dt = (m >> 2) & 1, dy = (m >> 1) & 1, dx = m & 1;
+            const int tile = ((pc.k - dt) * AY.n + (pc.i - dy)) * AX.n + (pc.j - dx);
+            const int xs = (dx ? AX.ext[pc.j - 1] - AX.blend[pc.j] : 0) + pc.x + bk * tp.wb;
+            const int ys = (dy ? AY.ext[pc.i - 1] - AY.blend[pc.i] : 0) + pc.y;
+            const int ts = NDIM == 3 ? (dt ? AT.ext[pc.k - 1] - AT.blend[pc.k] : 0) + pc.t : 0;
+            tma_load_4d(s_data + (uint32_t)n * node_bytes + (uint32_t)bk * box_bytes, &tp.maps[tile], xs, ys, ts,
+                        (int)pc.plane, bar);
+        }
+    }
+    bool ready = mbar_try_wait(bar, 0);
+    if (!ready) {
+        const uint64_t t0 = global_ns();
+        while (!(ready = mbar_try_wait(bar, 0)) && global_ns() - t0 < TB_TMA_WAIT_NS) {
+        }
+    }
+    if (!ready) {
+        if (threadIdx.x == 0 && tp.status != nullptr) atomicCAS(tp.status, (uint32_t)DEV_OK, (uint32_t)DEV_WAIT_TIMEOUT);
+        return;
+    }
+
+    int bdx, bdy, cpt;
+    box_layout(pc.wc, bdx, bdy, cpt);
+    const int tx = threadIdx.x % bdx;
+    const int ty = threadIdx.x / bdx;
+    if (ty >= bdy) return;
+    RowCtx<VEC> ctx;
+    ctx.stride = node_bytes;
+    if constexpr ((NEED & 4) != 0) {
+        ctx.wt = s_tw[pc.t];
+        ctx.ut = s_tu[pc.t];
+    }
+    const int64_t orow = (int64_t)p.OW * Elt<DT>::BYTES;
+    char* const obase = reinterpret_cast<char*>(p.out) +
+                        ((((pc.plane * p.OT + (NDIM == 3 ? AT.off[pc.k] + pc.t : 0)) * p.OH + AY.off[pc.i] + pc.y) *
+                              (int64_t)p.OW +
+                          AX.off[pc.j] + pc.x) *
+                         Elt<DT>::BYTES);
+    for (int q = 0; q < cpt; ++q) {
+        const int cc = tx + q * bdx;
+        if (cc >= pc.wc) break;
+        const int col = pc.x + cc * VEC;
+        if constexpr ((NEED & 1) != 0) {
+#pragma unroll
+            for (int l = 0; l < VEC; ++l) {
+                ctx.xw[l] = s_xw[col + l];
+                ctx.xu[l] = s_xu[col + l];
+            }
+        }
+        const int blk = cc / cpb;
+        const uint32_t cbase = s_data + (uint32_t)blk * box_bytes + (uint32_t)(cc - blk * cpb) * 16u;
+        for (int r = ty; r < pc.rows; r += bdy) {
+            ctx.base = cbase + (uint32_t)r * (uint32_t)tp.wb * Elt<DT>::BYTES;
+            if constexpr ((NEED & 2) != 0) {
+                ctx.wy = s_yw[pc.y + r];
+                ctx.uy = s_yu[pc.y + r];
+            }
+            C F[NN];
+            DagEval<NDIM, NEED, 3, DT, VEC>::run(ctx, F);
+            store_chunk<DT, VEC>(obase + r * orow + cc * 16, 0, F[0]);
+        }
+    }
+}
+
+template <int NDIM, int DT>
+__global__ void __launch_bounds__(STITCH_BLOCK) stitch_tma_kernel(const __grid_constant__ StitchTmaParams tp) {
+    pdl_trigger_dependents();
+    constexpr int VEC = 16 / Elt<DT>::BYTES;
+    extern __shared__ __align__(128) unsigned char s_dyn[];
+    const auto& p = tp.g;
+    const auto& AT = p.ax[0];
+    const auto& AY = p.ax[1];
+    const auto& AX = p.ax[2];
+
+    // which tile and plane (blockIdx.x, tile fastest), which piece (blockIdx.y)
+    TmaPiece pc;
+    const int ntiles = AX.n * AY.n * (NDIM == 3 ? AT.n : 1);
+    const int tile = (int)(blockIdx.x % (unsigned)ntiles);
+    pc.plane = (int64_t)(blockIdx.x / (unsigned)ntiles);
+    pc.j = tile % AX.n;
+    pc.i = (tile / AX.n) % AY.n;
+    pc.k = NDIM == 3 ? tile / (AX.n * AY.n) : 0;
+    const int Kt = NDIM == 3 ? AT.off[pc.k + 1] - AT.off[pc.k] : 1;
+    const int Ky = AY.off[pc.i + 1] - AY.off[pc.i];
+    const int Kx = AX.off[pc.j + 1] - AX.off[pc.j];
+    const int ebt = (NDIM == 3 && pc.k > 0) ? min(AT.blend[pc.k], Kt) : 0;
+    const int eby = pc.i > 0 ? min(AY.blend[pc.i], Ky) : 0;
+    const int ebx = pc.j > 0 ? min(AX.blend[pc.j], Kx) : 0;
+    int piece = blockIdx.y;
+    int need = -1;
+    constexpr int NB = NDIM == 3 ? 8 : 4;
+    for (int b = NB - 1; b >= 0; --b) {  // same order as tma_tile_pieces()
+        const BoxShape s = box_shape(b, Kt, Ky, Kx, ebt, eby, ebx, VEC);
+        if (s.nt <= 0 || s.ny <= 0 || s.width <= 0) continue;
+        const int np = tma_box_pieces(s, tp.rb, tp.wpc);
+        if (piece < np) {
+            const int ncb = (s.width + tp.wpc - 1) / tp.wpc;
+            const int nrb = (s.ny + tp.rb - 1) / tp.rb;
+            const int cb = piece % ncb;
+            const int rest = piece / ncb;
+            const int rbk = rest % nrb;
+            need = b;
+            pc.t = s.t0 + rest / nrb;
+            pc.y = s.y0 + rbk * tp.rb;
+            pc.rows = min(tp.rb, s.ny - rbk * tp.rb);
+            pc.x = s.x0 + cb * tp.wpc * VEC;
+            pc.wc = min(tp.wpc, s.width - cb * tp.wpc);
+            break;
+        }
+        piece -= np;
+    }
+    if (need < 0) return;  // this tile has fewer pieces than the grid row
+
+    // shared memory: mbarrier, band coefficients, then the staged sources
+    const uint32_t s_raw = (uint32_t)__cvta_generic_to_shared(s_dyn);
+    const uint32_t s_base = (s_raw + 127u) & ~127u;
+    const uint32_t bar = s_base;
+    float* s_coef = reinterpret_cast<float*>(s_dyn + (s_base - s_raw) + 128);
+    float* s_xw = s_coef;
+    float* s_xu = s_xw + ebx;
+    float* s_yw = s_xu + ebx;
+    float* s_yu = s_yw + eby;
+    float* s_tw = s_yu + eby;
+    float* s_tu = s_tw + ebt;
+    const uint32_t coef_bytes = (uint32_t)(2 * (ebx + eby + ebt)) * 4u;
+    const uint32_t s_data = (s_base + 128u + coef_bytes + 127u) & ~127u;
+    if (need & 1)
+        for (int c = threadIdx.x; c < ebx; c += blockDim.x) {
+            const float2 v = p.coef[AX.coef[pc.j] + c];
+            s_xw[c] = v.x;
+            s_xu[c] = v.y;
+        }
+    if (need & 2)
+        for (int c = threadIdx.x; c < eby; c += blockDim.x) {
+            const float2 v = p.coef[AY.coef[pc.i] + c];
+            s_yw[c] = v.x;
+            s_yu[c] = v.y;
+        }
+    if (need & 4)
+        for (int c = threadIdx.x; c < ebt; c += blockDim.x) {
+            const float2 v = p.coef[AT.coef[pc.k] + c];
+            s_tw[c] = v.x;
+            s_tu[c] = v.y;
+        }
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    // everything above read kernel parameters only; the tiles and the output
+    // may belong to the preceding grid
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+#define TB_TMA_ARGS tp, pc, s_xw, s_xu, s_yw, s_yu, s_tw, s_tu, bar, s_data
+    switch (need) {
+        case 0: run_box_tma<NDIM, 0, DT>(TB_TMA_ARGS); break;
+        case 1: run_box_tma<NDIM, 1, DT>(TB_TMA_ARGS); break;
+        case 2: run_box_tma<NDIM, 2, DT>(TB_TMA_ARGS); break;
+        case 3: run_box_tma<NDIM, 3, DT>(TB_TMA_ARGS); break;
+        default:
+            if constexpr (NDIM == 3) {
+                switch (need) {
+                    case 4: run_box_tma<NDIM, 4, DT>(TB_TMA_ARGS); break;
+                    case 5: run_box_tma<NDIM, 5, DT>(TB_TMA_ARGS); break;
+                    case 6: run_box_tma<NDIM, 6, DT>(TB_TMA_ARGS); break;
+                    case 7: run_box_tma<NDIM, 7, DT>(TB_TMA_ARGS); break;
+                }
+            }
+            break;
+    }
+#undef TB_TMA_ARGS
+}
+
 template <int MAXA, int MAXT, int MAXC>
 using KernelFn = void (*)(const StitchParams<MAXA, MAXT, MAXC>);
 
@@ -757,6 +1011,32 @@ cudaError_t launch_stitch_small(const StitchParamsSmall& p, const StitchLaunch& 
 
 cudaError_t launch_stitch_large(const StitchParamsLarge& p, const StitchLaunch& l, cudaStream_t s) {
     return launch(p, l, s);
+}
+
+cudaError_t launch_stitch_tma(const StitchTmaParams& p, const StitchLaunch& l, cudaStream_t s) {
+    void (*fn)(const StitchTmaParams);
+    if (l.ndim == 3) {
+        fn = l.dtype == F32 ? stitch_tma_kernel<3, F32> : l.dtype == F16 ? stitch_tma_kernel<3, F16>
+                                                                        : stitch_tma_kernel<3, BF16>;
+    } else {
+        fn = l.dtype == F32 ? stitch_tma_kernel<2, F32> : l.dtype == F16 ? stitch_tma_kernel<2, F16>
+                                                                        : stitch_tma_kernel<2, BF16>;
+    }
+    if (l.smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(l.grid_x, l.grid_y, l.grid_z);
+    cfg.blockDim = dim3(STITCH_BLOCK, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)l.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 }  // namespace tb

@@ -18,7 +18,9 @@ from typing import List, Optional, Sequence, Tuple
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libtileblend.so")
+# TILEBLEND_LIB selects another build of the same library (a variant built by
+# build.build(variant=...), e.g. with in-kernel bounds checks).
+LIB_PATH = os.environ.get("TILEBLEND_LIB") or os.path.join(_HERE, "_build", "libtileblend.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -100,6 +102,10 @@ _lib.tb_stitch3d_shard.restype = ctypes.c_int
 _lib.tb_stitch3d_shard.argtypes = [_P_vp, _vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _P_axis, _i32, _i32, _vp,
                                    _i64, _i64, _i64, _vp]
 
+_lib.tb_device_status.restype = ctypes.c_int
+_lib.tb_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), _i32]
+TB_DEV_OK, TB_DEV_WAIT_TIMEOUT, TB_DEV_OUT_OF_BOUNDS = 0, 1, 2
+
 _lib.tb_stitch2d_ramp.restype = ctypes.c_int
 _lib.tb_stitch2d_ramp.argtypes = [_P_vp, ctypes.c_int, _i64, _i64, ctypes.POINTER(tb_ramp_axis),
                                   ctypes.POINTER(tb_ramp_axis), _vp, _vp]
@@ -119,7 +125,7 @@ EXPORTED = ("tb_version", "tb_status_string", "tb_last_cuda_error", "tb_axis_lay
             "tb_stitch3d", "tb_stitch_shard_layout", "tb_stitch_halo_pack", "tb_stitch2d_shard",
             "tb_stitch3d_shard", "tb_stitch2d_ramp", "tb_patch_gn_stats", "tb_patch_gn_apply",
             "tb_patch_gn_apply_gathered", "tb_patch_group_norm_noalloc", "tb_patchify_layout", "tb_patchify",
-            "tb_gather_patches")
+            "tb_gather_patches", "tb_device_status")
 
 
 class TileBlendError(RuntimeError):
@@ -138,6 +144,13 @@ def _check(status: int, where: str) -> None:
 
 def tb_version() -> int:
     return int(_lib.tb_version())
+
+
+def tb_device_status(clear: bool = False) -> int:
+    """The device status word (0 = no kernel reported a problem); synchronises."""
+    v = ctypes.c_uint32(0)
+    _check(_lib.tb_device_status(ctypes.byref(v), 1 if clear else 0), "tb_device_status")
+    return int(v.value)
 
 
 # ---------------------------------------------------------------------------

@@ -281,3 +281,9 @@ def test_largest_tile_grid_bit_exact(tbl, ndim):
                    for lx in lays[2].extents] for ly in lays[1].extents] for lt in lays[0].extents]
     ref = oracle_stitch(_storage_grid(tiles, "bf16"), lays, "bf16")
     _check_equal(_run_gpu(tbl, tiles, axes, "bf16", 1, 2), ref, "bf16")
+
+
+def test_no_kernel_reported_a_problem(tbl):
+    # the device status word stays 0 through every stitch above (no copy
+    # wait ran out, no bounds check fired)
+    assert tbl.tb_device_status(clear=True) == tbl.TB_DEV_OK
