@@ -591,6 +591,14 @@ def run_profile_target(args):
         tdt = dt[0][0].dtype
         out = torch.empty((w.B, w.C, ay.out_extent, ax.out_extent), dtype=tdt, device=dev)
         launch = lambda: tb.tb_stitch2d_ramp(dt, ay, ax, out)
+    elif kernel == "copy":
+        # a plain copy of WORKLOAD megabytes (half read, half written) through
+        # the library's copy kernel: the single-launch reference for a
+        # streaming kernel of that many bytes
+        nbytes = int(float(name) * 1e6) // 2 // 16 * 16
+        xd = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev).fill_(1.0)
+        dst = [torch.empty_like(xd)]
+        launch = lambda: tb.tb_patchify(xd, 0, 1, 1, patches=dst)
     elif kernel in ("patchify", "gather_patches"):
         w = W.PATCHIFY[name]
         xd = W.make_patchify_input(w).to(dev)
@@ -741,7 +749,8 @@ def main():
     ap.add_argument("--kernels-only", default=None,
                     help="comma-separated workloads or kernel names: print only their per-kernel timings")
     ap.add_argument("--profile", default=None,
-                    help="KERNEL:WORKLOAD (stitch2d|stitch3d|gn_stats|gn_apply): plain launches for ncu")
+                    help="KERNEL:WORKLOAD (stitch2d|stitch3d|stitch2d_ramp|gn_stats|gn_apply|patchify|"
+                         "gather_patches, or copy:MEGABYTES): plain launches for ncu")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -307,6 +307,29 @@ typedef struct {
     const int64_t* origins;
 } tb_ramp_axis;
 
+/*
+ * tb_ramp_axis_spread -- one axis of a normalised-ramp layout as the Studio
+ * planner lays it out [STU], commit "Decode this VAE in 32-latent tiles
+ * ...": n_tiles tiles of latent_tile latents spread so the first starts at 0
+ * and the last ends at the canvas edge, tile n at
+ *     floor(n * (latent_extent - latent_tile) / (n_tiles - 1))  latents
+ * (the page does not say how the spread rounds; flooring is the reading
+ * taken), decoded at `scale` samples per latent, with a zero band of
+ * zero_latents and a ramp of ramp_latents latents (4 and 8 on the page).
+ * Host only.
+ *   origins  out: host array of n_tiles entries, the origins in samples
+ *   axis     out: the tb_ramp_axis for tb_stitch2d_ramp; axis->origins
+ *            points to `origins`
+ * Errors: TB_ERR_NULL; TB_ERR_GEOMETRY for n_tiles < 1, scale < 1,
+ * latent_tile outside [1, latent_extent], a single tile that is not the
+ * whole canvas, neighbouring origins further apart than a tile (samples
+ * no tile covers), zero_latents < 0 or ramp_latents < 1;
+ * TB_ERR_UNSUPPORTED for more than TB_MAX_TILES_PER_AXIS tiles or sizes
+ * past 2^31 samples.
+ */
+tb_status tb_ramp_axis_spread(int32_t latent_extent, int32_t latent_tile, int32_t n_tiles, int32_t scale,
+                              int32_t zero_latents, int32_t ramp_latents, int64_t* origins, tb_ramp_axis* axis);
+
 /* Most tiles with positive weight at one position of a ramp axis. */
 #define TB_RAMP_MAX_COVER 3
 

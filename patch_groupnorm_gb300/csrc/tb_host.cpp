@@ -45,7 +45,12 @@
 // sources with tensor copies (TMA), 0 always streams them through the
 // per-thread cp.async rings.
 #ifndef TB_STITCH_TMA
-#define TB_STITCH_TMA 1
+#define TB_STITCH_TMA 0
+#endif
+// L2 promotion of the TMA path's copies (CUtensorMapL2promotion: 0 none,
+// 1 64 B, 2 128 B, 3 256 B).
+#ifndef TB_TMA_L2_PROMOTION
+#define TB_TMA_L2_PROMOTION 3
 #endif
 // Rows of a TMA-path piece for 2-byte types (4-byte types take half).
 #ifndef TB_STITCH_TMA_ROWS
@@ -154,6 +159,16 @@ tb_status device_sms(int* sms) {
 }
 
 int elem_bytes(tb_dtype d) { return d == TB_F32 ? 4 : 2; }
+
+// The status word the bounds-checked build's kernels report to (null in the
+// product build, whose kernels make no checks).
+uint32_t* debug_status() {
+#if TB_DEBUG_BOUNDS
+    return tb::device_status_word();
+#else
+    return nullptr;
+#endif
+}
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -315,7 +330,8 @@ tb_status try_launch_tma(const tb::StitchParamsSmall& prm, const Axis (&g)[3], i
                 const cuuint32_t estr[4] = {1, 1, 1, 1};
                 if (encode(&tp.maps[q], dt, 4, const_cast<void*>(tiles[q]), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                           (CUtensorMapL2promotion)TB_TMA_L2_PROMOTION, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+                    CUDA_SUCCESS)
                     return TB_OK;
                 const int ebt = (ndim == 3 && k > 0) ? std::min(g[0].blend[k], g[0].kept[k]) : 0;
                 const int eby = i > 0 ? std::min(g[1].blend[i], g[1].kept[i]) : 0;
@@ -330,6 +346,9 @@ tb_status try_launch_tma(const tb::StitchParamsSmall& prm, const Axis (&g)[3], i
     for (int i = 1; i < g[1].n; ++i) max_eby = std::max(max_eby, std::min(g[1].blend[i], g[1].kept[i]));
     for (int k = 1; ndim == 3 && k < g[0].n; ++k) max_ebt = std::max(max_ebt, std::min(g[0].blend[k], g[0].kept[k]));
     const int64_t coef = (int64_t)(2 * (max_ebx + max_eby + max_ebt)) * 4;
+#ifdef TB_TMA_SMEM_CAP
+    if (sh.smem > TB_TMA_SMEM_CAP) return TB_OK;
+#endif
     tb::StitchLaunch l{};
     l.ndim = ndim;
     l.dtype = (int)dtype;
@@ -390,6 +409,7 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     const int ntiles = g[0].n * g[1].n * g[2].n;
     for (int q = 0; q < ntiles; ++q) prm.tiles[q] = tiles[q];
     prm.out = out;
+    prm.status = debug_status();
     prm.planes = planes;
     prm.OT = (int32_t)g[0].out;
     prm.OH = (int32_t)g[1].out;
@@ -731,6 +751,8 @@ tb_status patch_copy(bool to_patches, void* whole, void* const* patches, int32_t
     std::memset(&prm, 0, sizeof(prm));
     prm.whole = whole;
     prm.wpitch = chunks(extent * inner);
+    prm.outer = outer;
+    prm.status = debug_status();
     prm.P = P;
     const int64_t cta_chunks = tb::PF_CTA_BYTES / vec;
     int64_t ranges = 1;
@@ -967,6 +989,7 @@ TB_API tb_status tb_stitch_halo_pack(const void* const* tiles, tb_dtype dtype, i
     tb::HaloPackParams prm;
     std::memset(&prm, 0, sizeof(prm));
     prm.dst = halo;
+    prm.status = debug_status();
     prm.e = e;
     prm.ntiles = (int32_t)ntiles;
     const int64_t ly = g[1].ext[row];
@@ -984,6 +1007,7 @@ TB_API tb_status tb_stitch_halo_pack(const void* const* tiles, tb_dtype dtype, i
             off += prm.n[q];
             most = std::max(most, prm.n[q]);
         }
+    prm.dst_total = off;
     const int64_t cta = 16384 / vb;  // 16 KB per CTA
     prm.per_cta = cta;
     const int64_t ranges = (most + cta - 1) / cta;
@@ -1007,6 +1031,35 @@ TB_API tb_status tb_stitch3d_shard(const void* const* tiles, const void* halo, t
     if (at == nullptr) return TB_ERR_NULL;
     const Shard sh{row_begin, row_end, halo};
     return stitch_common(3, tiles, dtype, B, C, at, ay, ax, out, out_t, out_rows, out_w, stream, &sh);
+}
+
+TB_API tb_status tb_ramp_axis_spread(int32_t latent_extent, int32_t latent_tile, int32_t n_tiles, int32_t scale,
+                                     int32_t zero_latents, int32_t ramp_latents, int64_t* origins,
+                                     tb_ramp_axis* axis) {
+    if (origins == nullptr || axis == nullptr) return TB_ERR_NULL;
+    if (n_tiles < 1 || scale < 1 || latent_tile < 1 || latent_tile > latent_extent || zero_latents < 0 ||
+        ramp_latents < 1)
+        return TB_ERR_GEOMETRY;
+    if (n_tiles > TB_MAX_TILES_PER_AXIS) return TB_ERR_UNSUPPORTED;
+    if ((int64_t)latent_extent * scale > 2147483647LL || (int64_t)zero_latents * scale > 2147483647LL ||
+        (int64_t)ramp_latents * scale > 2147483647LL)
+        return TB_ERR_UNSUPPORTED;
+    if (n_tiles == 1 && latent_tile != latent_extent) return TB_ERR_GEOMETRY;
+    const int64_t span = (int64_t)latent_extent - latent_tile;
+    int64_t prev = 0;
+    for (int n = 0; n < n_tiles; ++n) {
+        const int64_t lat = n_tiles == 1 ? 0 : (int64_t)n * span / (n_tiles - 1);
+        if (n > 0 && lat - prev > latent_tile) return TB_ERR_GEOMETRY;
+        origins[n] = lat * scale;
+        prev = lat;
+    }
+    axis->n_tiles = n_tiles;
+    axis->tile_extent = latent_tile * scale;
+    axis->out_extent = latent_extent * scale;
+    axis->zero = zero_latents * scale;
+    axis->ramp = ramp_latents * scale;
+    axis->origins = origins;
+    return TB_OK;
 }
 
 TB_API tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
@@ -1050,6 +1103,7 @@ TB_API tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int6
     }
     for (int64_t q = 0; q < ntiles; ++q) prm.tiles[q] = tiles[q];
     prm.out = out;
+    prm.status = debug_status();
     prm.planes = planes;
     // A piece is a run of rows of one rectangle with every plane's rows laid
     // end to end, so rectangles a few rows high still fill whole CTAs.  Rows

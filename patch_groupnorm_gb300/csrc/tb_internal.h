@@ -35,6 +35,7 @@ struct StitchParams {
     void* out;                 // [planes, OT, OH, OW]
     int64_t planes;            // B * C
     int32_t OT, OH, OW;        // output extents
+    uint32_t* status;          // device status word (bounds-checked build), or null
     int32_t ncoef;             // used entries of coef[]
     int32_t rows_per_thread;   // work per thread in a box piece (tuning)
     StitchAxis<MAXA> ax[3];    // t, y, x
@@ -78,7 +79,40 @@ __host__ __device__ inline BoxShape box_shape(int b, int Kt, int Ky, int Kx, int
     return s;
 }
 
+#ifndef TB_DEBUG_BOUNDS
+#define TB_DEBUG_BOUNDS 0
+#endif
+
 #ifdef __CUDACC__
+// The bounds-checked build (TB_DEBUG_BOUNDS=1) checks every computed address
+// before it is read or written: true if the `bytes` at `addr` lie inside
+// [base, base + size); otherwise the first such finding is recorded in the
+// device status word (DEV_OUT_OF_BOUNDS, no trap) and the caller skips the
+// access.  In the product build the check compiles away.
+__device__ __forceinline__ bool in_bounds(const void* addr, int64_t bytes, const void* base, int64_t size,
+                                          uint32_t* status) {
+#if TB_DEBUG_BOUNDS
+    const char* a = static_cast<const char*>(addr);
+    const char* b = static_cast<const char*>(base);
+    if (base != nullptr && a >= b && bytes >= 0 && a + bytes <= b + size) return true;
+    if (status != nullptr) atomicCAS(status, 0u, 2u);
+    return false;
+#else
+    (void)addr, (void)bytes, (void)base, (void)size, (void)status;
+    return true;
+#endif
+}
+// Records DEV_OUT_OF_BOUNDS when `ok` is false (bounds-checked build only).
+__device__ __forceinline__ bool index_ok(bool ok, uint32_t* status) {
+#if TB_DEBUG_BOUNDS
+    if (!ok && status != nullptr) atomicCAS(status, 0u, 2u);
+    return ok;
+#else
+    (void)status;
+    return true;
+#endif
+}
+
 // Every kernel is launched with programmatic stream serialisation and runs
 // griddepcontrol.wait before its first global-memory access.  Triggering at
 // the start of each CTA lets the next kernel in the stream launch as soon as
@@ -160,7 +194,10 @@ cudaError_t launch_stitch_large(const StitchParamsLarge& p, const StitchLaunch& 
 // ---------------------------------------------------------------------------
 
 constexpr int TMA_MAXT = 128;            // tiles (one tensor map each)
-constexpr int TMA_SMEM_BUDGET = 64 * 1024;
+#ifndef TB_TMA_SMEM_BUDGET
+#define TB_TMA_SMEM_BUDGET (64 * 1024)
+#endif
+constexpr int TMA_SMEM_BUDGET = TB_TMA_SMEM_BUDGET;
 
 // A piece of box b (BoxShape s): one frame, `rb` rows, `wpc` chunks of
 // columns.  Pieces are numbered column block fastest, then row block, then
@@ -233,6 +270,7 @@ struct RampAxisK {
 struct RampParams {
     const void* tiles[1024];
     void* out;
+    uint32_t* status;   // device status word (bounds-checked build), or null
     int64_t planes;
     RampAxisK ay, ax;
     int32_t rows_per_piece[RAMP_MAXSEG];  // flattened (plane, row) rows per piece, by width segment
@@ -268,6 +306,8 @@ struct PatchCopyParams {
     int32_t step_o[PF_MAXP];   // PF_BLOCK / run[p]
     int32_t step_r[PF_MAXP];   // PF_BLOCK % run[p]
     int64_t wpitch;            // chunks per outer slice of the whole
+    int64_t outer;             // outer slices
+    uint32_t* status;          // device status word (bounds-checked build), or null
     int32_t P;
 };
 static_assert(sizeof(PatchCopyParams) <= 32000, "kernel parameter block too large");
@@ -293,6 +333,8 @@ struct HaloPackParams {
     int32_t width[HALO_MAXT];      // chunks per row of source tile q
     void* dst;
     int64_t per_cta;               // chunks one CTA copies
+    int64_t dst_total;             // chunks of the whole halo buffer
+    uint32_t* status;              // device status word (bounds-checked build), or null
     int32_t e;                     // band rows
     int32_t ntiles;
 };

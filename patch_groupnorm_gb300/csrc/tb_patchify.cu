@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(PF_BLOCK) patch_copy_kernel(const __grid_const
     const int64_t ppitch = p.ppitch[pi], wpitch = p.wpitch, woff = p.woff[pi];
     T* const pb = static_cast<T*>(p.patch[pi]);
     T* const wb = static_cast<T*>(p.whole);
+    const int64_t pbytes = p.outer * ppitch * V, wbytes = p.outer * wpitch * V;  // bounds-checked build
     // The previous kernel on the stream (launched with programmatic
     // serialisation) may still be writing what this one reads.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -81,7 +82,9 @@ __global__ void __launch_bounds__(PF_BLOCK) patch_copy_kernel(const __grid_const
             if (c < c1) {
                 T* const at_patch = pb + ((int64_t)o * ppitch + r);
                 T* const at_whole = wb + ((int64_t)o * wpitch + woff + r);
-                if (TO_PATCHES) {
+                if (!in_bounds(at_patch, V, pb, pbytes, p.status) || !in_bounds(at_whole, V, wb, wbytes, p.status)) {
+                    // skipped (bounds-checked build only)
+                } else if (TO_PATCHES) {
                     v[u] = __ldg(at_whole);
                     dst[u] = at_patch;
                 } else {

@@ -185,13 +185,18 @@ __device__ __forceinline__ void run_rect(const RampParams& p, int sy, int sx, in
         // sources: tile (Y.tile[a], X.tile[b]) at plane 0, canvas row y0
         const int y0 = AY.seg_start[sy];
         const char* src[NU];
+        const char* tbase[NU];  // the bounds-checked build's source ranges
         const int32_t pitch = AX.T * RElt<DT>::BYTES;
         const int64_t tplane = (int64_t)AY.T * AX.T * RElt<DT>::BYTES;
+        const int64_t tbytes = p.planes * tplane;
+        const int64_t obytes = p.planes * (int64_t)AY.out * AX.out * RElt<DT>::BYTES;
 #pragma unroll
         for (int a = 0; a < CY; ++a)
 #pragma unroll
             for (int b = 0; b < CX; ++b) {
                 const int ti = AY.seg_tile[sy][a], tj = AX.seg_tile[sx][b];
+                index_ok(ti >= 0 && ti < AY.n && tj >= 0 && tj < AX.n, p.status);
+                tbase[a * CX + b] = reinterpret_cast<const char*>(p.tiles[ti * AX.n + tj]);
                 // element (plane, y0 + yl - oy, x0 - ox) of tile (ti, tj) is
                 // src + plane * tplane + yl * pitch
                 src[a * CX + b] = reinterpret_cast<const char*>(p.tiles[ti * AX.n + tj]) +
@@ -245,7 +250,9 @@ __device__ __forceinline__ void run_rect(const RampParams& p, int sy, int sx, in
                 const int64_t off = ahead.plane * tplane + (int64_t)ahead.yl * pitch;
                 const uint32_t st = my_slot + (uint32_t)((m % S) * NU) * slot_stride;
 #pragma unroll
-                for (int n = 0; n < NU; ++n) cp_async16(st + (uint32_t)n * slot_stride, src[n] + off);
+                for (int n = 0; n < NU; ++n)
+                    if (in_bounds(src[n] + off, 16, tbase[n], tbytes, p.status))
+                        cp_async16(st + (uint32_t)n * slot_stride, src[n] + off);
                 ahead.advance(sq, sr, len);
             };
 #pragma unroll
@@ -268,7 +275,8 @@ __device__ __forceinline__ void run_rect(const RampParams& p, int sy, int sx, in
                         unpack_chunk<DT, VEC>(v, x);
                     });
                 }
-                __stcs(reinterpret_cast<uint4*>(dst + at.plane * oplane + (int64_t)at.yl * opitch), o);
+                char* const ot = dst + at.plane * oplane + (int64_t)at.yl * opitch;
+                if (in_bounds(ot, 16, p.out, obytes, p.status)) __stcs(reinterpret_cast<uint4*>(ot), o);
                 at.advance(sq, sr, len);
             }
             cp_async_wait<0>();
@@ -278,13 +286,18 @@ __device__ __forceinline__ void run_rect(const RampParams& p, int sy, int sx, in
             for (int m = 0; m < nrows; ++m) {
                 const int64_t off = at.plane * tplane + (int64_t)at.yl * pitch;
                 char* const o_at = dst + at.plane * oplane + (int64_t)at.yl * opitch;
+                const bool store_ok = in_bounds(o_at, RElt<DT>::BYTES, p.out, obytes, p.status);
                 if constexpr (NU == 1) {
-                    store_elem<DT>(o_at, load_elem<DT>(src[0] + off));
+                    if (store_ok && in_bounds(src[0] + off, RElt<DT>::BYTES, tbase[0], tbytes, p.status))
+                        store_elem<DT>(o_at, load_elem<DT>(src[0] + off));
                 } else {
                     const uint4 o = combine(y0 + at.yl, [&](int a, int b, float (&x)[VEC]) {
-                        x[0] = elem_value<DT>(load_elem<DT>(src[a * CX + b] + off));
+                        const char* at_src = src[a * CX + b] + off;
+                        x[0] = in_bounds(at_src, RElt<DT>::BYTES, tbase[a * CX + b], tbytes, p.status)
+                                   ? elem_value<DT>(load_elem<DT>(at_src))
+                                   : 0.f;
                     });
-                    store_elem<DT>(o_at, o.x);
+                    if (store_ok) store_elem<DT>(o_at, o.x);
                 }
                 at.advance(sq, sr, len);
             }

@@ -54,12 +54,16 @@ __global__ void __launch_bounds__(HALO_BLOCK) halo_pack_kernel(const __grid_cons
     const uint64_t L = (uint64_t)p.rows[q];
     const T* src = reinterpret_cast<const T*>(p.src[q]);
     T* dst = reinterpret_cast<T*>(p.dst) + p.dst_off[q];
+    const int64_t src_bytes = n / (int64_t)e * (int64_t)L * VB;  // bounds-checked build
     for (int64_t c = c0 + threadIdx.x; c < c1; c += HALO_BLOCK) {
         const uint64_t r = (uint64_t)c / w;      // (plane, frame, band row), flattened
         const uint64_t x = (uint64_t)c - r * w;
         const uint64_t fp = r / e;               // (plane, frame)
         const uint64_t row = r - fp * e;
-        dst[c] = __ldcs(src + (fp * L + (L - e + row)) * w + x);
+        const T* at = src + (fp * L + (L - e + row)) * w + x;
+        if (in_bounds(at, VB, src, src_bytes, p.status) &&
+            in_bounds(dst + c, VB, p.dst, p.dst_total * VB, p.status))
+            dst[c] = __ldcs(at);
     }
 }
 

@@ -279,6 +279,58 @@ __device__ __forceinline__ const char* node_origin(const StitchParams<MAXA, MAXT
            (((pc.plane * Lt + lt) * Ly + ly) * Lx + lx) * Elt<DT>::BYTES;
 }
 
+// The tile node m of the box reads, as a byte range, for the bounds-checked
+// build (empty otherwise); the node's tile indices are checked too.
+struct Span {
+#if TB_DEBUG_BOUNDS
+    const char* base;
+    int64_t size;
+#endif
+};
+
+template <int NDIM, int DT, int MAXA, int MAXT, int MAXC>
+__device__ __forceinline__ Span node_span(const StitchParams<MAXA, MAXT, MAXC>& p, const Piece& pc, int m) {
+    Span sp;
+#if TB_DEBUG_BOUNDS
+    const auto& AT = p.ax[0];
+    const auto& AY = p.ax[1];
+    const auto& AX = p.ax[2];
+    const int kq = pc.k - ((m >> 2) & 1), iq = pc.i - ((m >> 1) & 1), jq = pc.j - (m & 1);
+    const bool ok = kq >= 0 && kq < (NDIM == 3 ? AT.n : 1) && iq >= 0 && iq < AY.n && jq >= 0 && jq < AX.n;
+    if (!index_ok(ok, p.status)) {
+        sp.base = nullptr;
+        sp.size = 0;
+        return sp;
+    }
+    sp.base = reinterpret_cast<const char*>(p.tiles[(kq * AY.n + iq) * AX.n + jq]);
+    sp.size = p.planes * (NDIM == 3 ? AT.ext[kq] : 1) * (int64_t)AY.ext[iq] * AX.ext[jq] * Elt<DT>::BYTES;
+#else
+    (void)p, (void)pc, (void)m;
+#endif
+    return sp;
+}
+
+template <int DT, int MAXA, int MAXT, int MAXC>
+__device__ __forceinline__ Span out_span(const StitchParams<MAXA, MAXT, MAXC>& p) {
+    Span sp;
+#if TB_DEBUG_BOUNDS
+    sp.base = reinterpret_cast<const char*>(p.out);
+    sp.size = p.planes * p.OT * (int64_t)p.OH * p.OW * Elt<DT>::BYTES;
+#else
+    (void)p;
+#endif
+    return sp;
+}
+
+__device__ __forceinline__ bool span_ok(const Span& sp, const void* a, int64_t bytes, uint32_t* status) {
+#if TB_DEBUG_BOUNDS
+    return in_bounds(a, bytes, sp.base, sp.size, status);
+#else
+    (void)sp, (void)a, (void)bytes, (void)status;
+    return true;
+#endif
+}
+
 // Byte pitches of one frame and one row in the source tiles: row pitch by
 // width-neighbour bit dx, frame pitch by (dy, dx).
 struct Pitches {
@@ -371,10 +423,15 @@ __device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p,
             }
         }
         const char* org[NN];
+        Span span[NN];
 #pragma unroll
         for (int m = 0; m < NN; ++m)
-            if ((m & ~NEED) == 0) org[m] = node_origin<NDIM, DT>(p, pc, m, cx);
+            if ((m & ~NEED) == 0) {
+                org[m] = node_origin<NDIM, DT>(p, pc, m, cx);
+                span[m] = node_span<NDIM, DT>(p, pc, m);
+            }
         char* oorg = out_origin<NDIM, DT>(p, pc, cx);
+        const Span ospan = out_span<DT>(p);
         for (int r = pc.rbeg + ty; r < pc.rend; r += UR * pc.bdy) {
             C F[UR][NN];
             RowPos<NDIM> pos[UR];
@@ -387,7 +444,8 @@ __device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p,
                     for (int m = 0; m < NN; ++m) {
                         if ((m & ~NEED) != 0) continue;
                         const int dy = (m >> 1) & 1, dx = m & 1;
-                        F[u][m] = load_chunk<DT, VEC>(org[m] + pos[u].off(pt.frame[dy][dx], pt.row[dx]), 0);
+                        const char* at = org[m] + pos[u].off(pt.frame[dy][dx], pt.row[dx]);
+                        if (span_ok(span[m], at, VEC * Elt<DT>::BYTES, p.status)) F[u][m] = load_chunk<DT, VEC>(at, 0);
                     }
                 }
             }
@@ -408,7 +466,8 @@ __device__ __forceinline__ void run_box(const StitchParams<MAXA, MAXT, MAXC>& p,
                         eval_nodes<NDIM, NEED, DT, VEC>(F[u], wt, ut, wy, uy, [&](int l) { return xw[l]; },
                                                         [&](int l) { return xu[l]; });
                     }
-                    store_chunk<DT, VEC>(oorg + pos[u].off(pt.oframe, pt.orow), 0, F[u][0]);
+                    char* const ot = oorg + pos[u].off(pt.oframe, pt.orow);
+                    if (span_ok(ospan, ot, VEC * Elt<DT>::BYTES, p.status)) store_chunk<DT, VEC>(ot, 0, F[u][0]);
                 }
             }
         }
@@ -531,10 +590,15 @@ __device__ __forceinline__ void run_box_pipe(const StitchParams<MAXA, MAXT, MAXC
             }
         }
         const char* org[NU];
+        Span span[NU];
 #pragma unroll
         for (int m = 0; m < NN; ++m)
-            if ((m & ~NEED) == 0) org[node_rank(NEED, m)] = node_origin<NDIM, DT>(p, pc, m, cx);
+            if ((m & ~NEED) == 0) {
+                org[node_rank(NEED, m)] = node_origin<NDIM, DT>(p, pc, m, cx);
+                span[node_rank(NEED, m)] = node_span<NDIM, DT>(p, pc, m);
+            }
         char* oorg = out_origin<NDIM, DT>(p, pc, cx);
+        const Span ospan = out_span<DT>(p);
 
         const int r0 = pc.rbeg + ty;
         const int nrows = r0 < pc.rend ? (pc.rend - r0 + pc.bdy - 1) / pc.bdy : 0;
@@ -548,7 +612,8 @@ __device__ __forceinline__ void run_box_pipe(const StitchParams<MAXA, MAXT, MAXC
                 if ((mm & ~NEED) != 0) continue;
                 const int dy = (mm >> 1) & 1, dx = mm & 1;
                 const int n = node_rank(NEED, mm);
-                cp_async16(st + (uint32_t)n * slot_stride, org[n] + ipos.off(pt.frame[dy][dx], pt.row[dx]));
+                const char* at = org[n] + ipos.off(pt.frame[dy][dx], pt.row[dx]);
+                if (span_ok(span[n], at, 16, p.status)) cp_async16(st + (uint32_t)n * slot_stride, at);
             }
             ipos.advance(pc.bdy, pc.nyb);
         };
@@ -572,7 +637,8 @@ __device__ __forceinline__ void run_box_pipe(const StitchParams<MAXA, MAXT, MAXC
             }
             C F[NN];
             DagEval<NDIM, NEED, 3, DT, VEC>::run(ctx, F);
-            store_chunk<DT, VEC>(oorg + cpos.off(pt.oframe, pt.orow), 0, F[0]);
+            char* const ot = oorg + cpos.off(pt.oframe, pt.orow);
+            if (span_ok(ospan, ot, 16, p.status)) store_chunk<DT, VEC>(ot, 0, F[0]);
             cpos.advance(pc.bdy, pc.nyb);
         }
         cp_async_wait<0>();
@@ -818,6 +884,7 @@ __device__ __forceinline__ void run_box_tma(const StitchTmaParams& tp, const Tma
         ctx.ut = s_tu[pc.t];
     }
     const int64_t orow = (int64_t)p.OW * Elt<DT>::BYTES;
+    const Span ospan = out_span<DT>(p);
     char* const obase = reinterpret_cast<char*>(p.out) +
                         ((((pc.plane * p.OT + (NDIM == 3 ? AT.off[pc.k] + pc.t : 0)) * p.OH + AY.off[pc.i] + pc.y) *
                               (int64_t)p.OW +
@@ -844,13 +911,22 @@ __device__ __forceinline__ void run_box_tma(const StitchTmaParams& tp, const Tma
             }
             C F[NN];
             DagEval<NDIM, NEED, 3, DT, VEC>::run(ctx, F);
-            store_chunk<DT, VEC>(obase + r * orow + cc * 16, 0, F[0]);
+            char* const ot = obase + r * orow + cc * 16;
+            if (span_ok(ospan, ot, 16, p.status)) store_chunk<DT, VEC>(ot, 0, F[0]);
         }
     }
 }
 
+#ifndef TB_TMA_MIN_CTAS
+#define TB_TMA_MIN_CTAS 1
+#endif
+#ifndef TB_TMA_PREFETCH
+#define TB_TMA_PREFETCH 1
+#endif
+
 template <int NDIM, int DT>
-__global__ void __launch_bounds__(STITCH_BLOCK) stitch_tma_kernel(const __grid_constant__ StitchTmaParams tp) {
+__global__ void __launch_bounds__(STITCH_BLOCK, TB_TMA_MIN_CTAS)
+    stitch_tma_kernel(const __grid_constant__ StitchTmaParams tp) {
     pdl_trigger_dependents();
     constexpr int VEC = 16 / Elt<DT>::BYTES;
     extern __shared__ __align__(128) unsigned char s_dyn[];
@@ -897,6 +973,17 @@ __global__ void __launch_bounds__(STITCH_BLOCK) stitch_tma_kernel(const __grid_c
         piece -= np;
     }
     if (need < 0) return;  // this tile has fewer pieces than the grid row
+#if TB_TMA_PREFETCH
+    // the tensor maps of the (up to 2^d) source tiles, ahead of their copies
+    if (threadIdx.x < (1 << NDIM)) {
+        const int m = threadIdx.x;
+        const int dt = (m >> 2) & 1, dy = (m >> 1) & 1, dx = m & 1;
+        if ((m & ~need) == 0) {
+            const CUtensorMap* map = &tp.maps[((pc.k - dt) * AY.n + (pc.i - dy)) * AX.n + (pc.j - dx)];
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+        }
+    }
+#endif
 
     // shared memory: mbarrier, band coefficients, then the staged sources
     const uint32_t s_raw = (uint32_t)__cvta_generic_to_shared(s_dyn);

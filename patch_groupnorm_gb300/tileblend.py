@@ -106,6 +106,8 @@ _lib.tb_device_status.restype = ctypes.c_int
 _lib.tb_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), _i32]
 TB_DEV_OK, TB_DEV_WAIT_TIMEOUT, TB_DEV_OUT_OF_BOUNDS = 0, 1, 2
 
+_lib.tb_ramp_axis_spread.restype = ctypes.c_int
+_lib.tb_ramp_axis_spread.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _P_i64, ctypes.POINTER(tb_ramp_axis)]
 _lib.tb_stitch2d_ramp.restype = ctypes.c_int
 _lib.tb_stitch2d_ramp.argtypes = [_P_vp, ctypes.c_int, _i64, _i64, ctypes.POINTER(tb_ramp_axis),
                                   ctypes.POINTER(tb_ramp_axis), _vp, _vp]
@@ -125,7 +127,7 @@ EXPORTED = ("tb_version", "tb_status_string", "tb_last_cuda_error", "tb_axis_lay
             "tb_stitch3d", "tb_stitch_shard_layout", "tb_stitch_halo_pack", "tb_stitch2d_shard",
             "tb_stitch3d_shard", "tb_stitch2d_ramp", "tb_patch_gn_stats", "tb_patch_gn_apply",
             "tb_patch_gn_apply_gathered", "tb_patch_group_norm_noalloc", "tb_patchify_layout", "tb_patchify",
-            "tb_gather_patches", "tb_device_status")
+            "tb_gather_patches", "tb_device_status", "tb_ramp_axis_spread")
 
 
 class TileBlendError(RuntimeError):
@@ -413,12 +415,13 @@ class RampAxis:
     @staticmethod
     def spread(latent_extent: int, latent_tile: int, n_tiles: int, scale: int, zero_latents: int = 4,
                ramp_latents: int = 8) -> "RampAxis":
-        """n_tiles tiles spread so the first starts at 0 and the last ends at
-        the edge: tile n at floor(n * (latent_extent - latent_tile) /
-        (n_tiles - 1)) latents."""
-        span = latent_extent - latent_tile
-        org = tuple(0 if n_tiles == 1 else (n * span // (n_tiles - 1)) * scale for n in range(n_tiles))
-        return RampAxis(org, latent_tile * scale, latent_extent * scale, zero_latents * scale, ramp_latents * scale)
+        """The library's layout of n_tiles tiles spread edge to edge
+        (tb_ramp_axis_spread)."""
+        org = (ctypes.c_int64 * max(1, n_tiles))()
+        a = tb_ramp_axis()
+        _check(_lib.tb_ramp_axis_spread(latent_extent, latent_tile, n_tiles, scale, zero_latents, ramp_latents, org,
+                                        ctypes.byref(a)), "tb_ramp_axis_spread")
+        return RampAxis(tuple(org[:n_tiles]), a.tile_extent, a.out_extent, a.zero, a.ramp)
 
     def c(self):
         arr = (ctypes.c_int64 * len(self.origins))(*self.origins)

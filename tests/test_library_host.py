@@ -364,3 +364,42 @@ def test_gathered_apply_rejects_before_launch(tbl):
     assert g(ptrs, ptrs, 1, 2, 1, 64, sp, 32, 16, 65537, None, None, eps, 1, None) == tbl.TB_ERR_UNSUPPORTED
     assert g(ptrs, ptrs, 1, 2, 1, 64, sp, 32, None, 4, None, None, eps, 1, None) == tbl.TB_ERR_NULL
     assert g(ptrs, ptrs, 1, 2, 1, 60, sp, 32, 16, 4, None, None, eps, 1, None) == tbl.TB_ERR_SHAPE     # C % G
+
+
+def test_ramp_spread_matches_the_oracle_on_every_tile():
+    # the library's planner spread against the oracle's, interior tiles included
+    import random
+    from oracle.ramp import evenly_spread_origins
+    from patch_groupnorm_gb300 import build
+    build.build()
+    from patch_groupnorm_gb300 import tileblend as tbl
+    rnd = random.Random(5)
+    checked = 0
+    for _ in range(500):
+        tile = rnd.randint(2, 80)
+        ext = rnd.randint(tile, 10 * tile)
+        n = 1 if ext == tile else rnd.randint(2, 20)
+        if n > 1 and -(-(ext - tile) // (n - 1)) > tile:
+            continue                                   # would leave a gap: refused, checked below
+        scale = rnd.choice([1, 2, 8, 16])
+        got = tbl.RampAxis.spread(ext, tile, n, scale)
+        assert list(got.origins) == evenly_spread_origins(ext, tile, n, scale)
+        assert (got.tile_extent, got.out_extent, got.zero, got.ramp) == (tile * scale, ext * scale, 4 * scale,
+                                                                         8 * scale)
+        checked += 1
+    assert checked > 300
+
+
+def test_ramp_spread_rejects_bad_layouts(tbl):
+    org = (ctypes.c_int64 * 64)()
+    a = tbl.tb_ramp_axis()
+    f = tbl._lib.tb_ramp_axis_spread
+    assert f(100, 32, 0, 8, 4, 8, org, ctypes.byref(a)) == tbl.TB_ERR_GEOMETRY      # no tiles
+    assert f(100, 32, 1, 8, 4, 8, org, ctypes.byref(a)) == tbl.TB_ERR_GEOMETRY      # one tile, not the canvas
+    assert f(100, 32, 2, 8, 4, 8, org, ctypes.byref(a)) == tbl.TB_ERR_GEOMETRY      # a 36-latent gap
+    assert f(100, 132, 4, 8, 4, 8, org, ctypes.byref(a)) == tbl.TB_ERR_GEOMETRY     # tile past the canvas
+    assert f(100, 32, 4, 8, 4, 0, org, ctypes.byref(a)) == tbl.TB_ERR_GEOMETRY      # no ramp
+    assert f(10000, 32, 65, 8, 4, 8, org, ctypes.byref(a)) == tbl.TB_ERR_UNSUPPORTED
+    assert f(100, 32, 4, 8, 4, 8, None, ctypes.byref(a)) == tbl.TB_ERR_NULL
+    assert f(100, 32, 4, 8, 4, 8, org, ctypes.byref(a)) == tbl.TB_OK
+    assert list(org[:4]) == [0, 22 * 8, 45 * 8, 68 * 8] and a.n_tiles == 4

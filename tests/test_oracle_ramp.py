@@ -90,3 +90,28 @@ def test_a_pixel_without_weight_is_refused():
         # overlap too short for the zero bands: the seam has no weight
         t = _tiles(np.random.default_rng(4), [0], [0, 30], 4, 36)
         ramp_stitch_2d(t, [0], [0, 30], 4, 36, (4, 66), 0, 1, 4, 8)
+
+
+def test_spread_is_even_edge_to_edge_and_covering():
+    # what the page fixes about the spread: the first tile at 0, the last
+    # ending at the edge, and the tiles equally spaced -- in whole latents the
+    # gaps can differ by one at most -- with no sample left uncovered
+    import random
+    rnd = random.Random(17)
+    for _ in range(400):
+        tile = rnd.randint(4, 96)
+        ext = rnd.randint(tile, 12 * tile)
+        lo = 1 if ext == tile else 2
+        n = rnd.randint(lo, lo + 10)
+        if n == 1:
+            continue
+        scale = rnd.choice([1, 8, 16])
+        org = evenly_spread_origins(ext, tile, n, scale)
+        lat = [o // scale for o in org]
+        assert all(o % scale == 0 for o in org)
+        assert lat[0] == 0 and lat[-1] + tile == ext
+        gaps = [b - a for a, b in zip(lat, lat[1:])]
+        assert max(gaps) - min(gaps) <= 1
+        assert sum(gaps) == ext - tile
+        # the spread never runs ahead of the exact equal spacing
+        assert all(l * (n - 1) <= k * (ext - tile) for k, l in enumerate(lat))
