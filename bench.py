@@ -406,28 +406,37 @@ def per_kernel(torch, tb, W, dev, peak, reps, only=None):
     CUDA graph and replayed back to back, so host call overhead is excluded;
     per-launch time = replay time / launches (median of reps).
     single: one launch at a time, cold: before each, a 258 MB fill evicts L2
-    and the GPU then spins for about 2 ms, long enough for the host to queue
-    the start event, the launch and the end event behind it, so the events
-    bracket the launch alone and no host time is timed; median of reps.
-    This is the figure comparable with ncu's serialised gpu__time_duration."""
+    and the GPU then spins for about 2 ms while the host queues the start
+    event, a graph holding that one launch, and the end event, so the events
+    bracket the launch alone (no host time); median of reps.  This is the
+    figure comparable with ncu's serialised gpu__time_duration."""
     stream = torch.cuda.Stream(dev)
     res = []
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
     def single_ms(launch_set, nsets):
+        # each set's launch alone in a graph, replayed after the flush and a
+        # GPU spin (the host's call and launch overheads stay outside)
+        graphs = []
+        for q in range(nsets):
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=stream):
+                launch_set(q)
+            graphs.append(g1)
+        cur = torch.cuda.current_stream(dev)
         ts = []
-        with torch.cuda.stream(stream):
-            for r in range(reps + 2):
-                flush.fill_(float(r))
-                torch.cuda._sleep(4_000_000)     # ~2 ms at 2 GHz: the host queues what follows
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                launch_set(r % nsets)
-                b.record(stream)
-                b.synchronize()
-                if r >= 2:
-                    ts.append(a.elapsed_time(b))
+        for r in range(reps + 2):
+            flush.fill_(float(r))
+            torch.cuda._sleep(4_000_000)     # ~2 ms at 2 GHz: the host queues what follows
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(cur)
+            graphs[r % nsets].replay()
+            b.record(cur)
+            b.synchronize()
+            if r >= 2:
+                ts.append(a.elapsed_time(b))
+        del graphs
         return statistics.median(ts)
 
     def timed(launch_set, nsets, nbytes, name, workload, per_graph=60):

@@ -290,29 +290,40 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
             // Groups of STATS_GROUP chunks: shifted sums about the group's
             // first element on packed fp32 pairs (3 packed operations per
             // element pair), then one Chan merge per group.
+            // The loop runs one group per iteration, unrolled: a group starts
+            // on ring slot 0, so every slot index is a constant, and the
+            // address of the chunk fetched ahead steps by a constant.
+            static_assert(STATS_GROUP % STATS_SLOTS == 0, "a group must start on ring slot 0");
             unsigned long long s1 = 0, s2 = 0, k2 = 0;
             float K = 0.f;
-            for (int k = 0; k < cnt; ++k) {
-                const int ahead = k + STATS_SLOTS - 1;
-                if (ahead < cnt)
-                    cp_async16(ring + (ahead % STATS_SLOTS) * SLOT, src + first + (int64_t)ahead * STATS_BLOCK);
-                cp_async_commit();
-                cp_async_wait<STATS_SLOTS - 1>();
-                const uint4 v = lds16(ring + (k % STATS_SLOTS) * SLOT);
-                if ((k % STATS_GROUP) == 0) {
-                    if (k > 0) acc = chan_fast(acc, shifted_stat(s1, s2, K, (float)(STATS_GROUP * VEC)));
-                    K = GElt<DT>::to_f(v.x);
-                    const unsigned long long kb = __float_as_uint(K);
-                    k2 = kb | (kb << 32);
-                    s1 = 0;
-                    s2 = 0;
+            const uint4* next = src + first + (int64_t)(STATS_SLOTS - 1) * STATS_BLOCK;  // chunk k + SLOTS - 1
+            for (int k0 = 0; k0 < cnt; k0 += STATS_GROUP) {
+                const int m = min(STATS_GROUP, cnt - k0);
+#pragma unroll
+                for (int u = 0; u < STATS_GROUP; ++u) {
+                    if (u < m) {
+                        if (k0 + u + STATS_SLOTS - 1 < cnt)
+                            cp_async16(ring + ((u + STATS_SLOTS - 1) % STATS_SLOTS) * SLOT, next);
+                        next += STATS_BLOCK;
+                        cp_async_commit();
+                        cp_async_wait<STATS_SLOTS - 1>();
+                        const uint4 v = lds16(ring + (u % STATS_SLOTS) * SLOT);
+                        if (u == 0) {
+                            K = GElt<DT>::to_f(v.x);
+                            const unsigned long long kb = __float_as_uint(K);
+                            k2 = kb | (kb << 32);
+                            s1 = 0;
+                            s2 = 0;
+                        }
+                        shifted_acc<DT>(v.x, k2, s1, s2);
+                        shifted_acc<DT>(v.y, k2, s1, s2);
+                        shifted_acc<DT>(v.z, k2, s1, s2);
+                        shifted_acc<DT>(v.w, k2, s1, s2);
+                    }
                 }
-                shifted_acc<DT>(v.x, k2, s1, s2);
-                shifted_acc<DT>(v.y, k2, s1, s2);
-                shifted_acc<DT>(v.z, k2, s1, s2);
-                shifted_acc<DT>(v.w, k2, s1, s2);
+                // merging into the empty triple of the first group is exact
+                acc = chan_fast(acc, shifted_stat(s1, s2, K, (float)(m * VEC)));
             }
-            if (cnt > 0) acc = chan_fast(acc, shifted_stat(s1, s2, K, (float)(((cnt - 1) % STATS_GROUP + 1) * VEC)));
         } else {
             for (int k = 0; k < cnt; ++k) {
                 const int ahead = k + STATS_SLOTS - 1;

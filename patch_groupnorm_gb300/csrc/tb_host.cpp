@@ -56,6 +56,23 @@
 #ifndef TB_STITCH_TMA_ROWS
 #define TB_STITCH_TMA_ROWS 32
 #endif
+// Grids sized to one wave: a stitch small enough to run in a few waves takes
+// the rows per thread that fill one wave of TB_STITCH_WAVE_CTAS CTAs per SM
+// best; the GroupNorm statistics take the part count that fills one wave of
+// TB_GN_WAVE_CTAS CTAs per SM best.  A lone launch then has no partial last
+// wave.  0 keeps the fixed choices.
+#ifndef TB_STITCH_WAVE_FIT
+#define TB_STITCH_WAVE_FIT 0
+#endif
+#ifndef TB_STITCH_WAVE_CTAS
+#define TB_STITCH_WAVE_CTAS 4
+#endif
+#ifndef TB_GN_WAVE_FIT
+#define TB_GN_WAVE_FIT 0
+#endif
+#ifndef TB_GN_WAVE_CTAS
+#define TB_GN_WAVE_CTAS 5
+#endif
 // CTAs per GroupNorm statistics unit (a power of two dividing TB_GN_PARTS);
 // 0 picks it from the sizes and the SM count.
 #ifndef TB_GN_FORCE_PARTS
@@ -429,19 +446,54 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     l.dtype = (int)dtype;
     l.vec = vec;
     // Pieces per tile; the grid's second extent is the largest count.
-    const int rpt = ndim == 3 ? TB_STITCH_ROWS_PER_THREAD_3D : TB_STITCH_ROWS_PER_THREAD;
-    int max_pieces = 0, max_ebx = 0, max_eby = 0;
-    for (int k = 0; k < g[0].n; ++k)
-        for (int i = 0; i < g[1].n; ++i)
-            for (int j = 0; j < g[2].n; ++j) {
-                const int ebt = (ndim == 3 && k > 0) ? std::min(g[0].blend[k], g[0].kept[k]) : 0;
-                const int eby = i > 0 ? std::min(g[1].blend[i], g[1].kept[i]) : 0;
-                const int ebx = j > 0 ? std::min(g[2].blend[j], g[2].kept[j]) : 0;
-                max_ebx = std::max(max_ebx, ebx);
-                max_eby = std::max(max_eby, eby);
-                max_pieces = std::max(max_pieces, tb::tile_pieces(ndim, g[0].kept[k], g[1].kept[i], g[2].kept[j],
-                                                                  ebt, eby, ebx, vec, rpt));
+    int rpt = ndim == 3 ? TB_STITCH_ROWS_PER_THREAD_3D : TB_STITCH_ROWS_PER_THREAD;
+    auto count = [&](int r, int& max_p, int64_t& total) {
+        max_p = 0;
+        total = 0;
+        for (int k = 0; k < g[0].n; ++k)
+            for (int i = 0; i < g[1].n; ++i)
+                for (int j = 0; j < g[2].n; ++j) {
+                    const int ebt = (ndim == 3 && k > 0) ? std::min(g[0].blend[k], g[0].kept[k]) : 0;
+                    const int eby = i > 0 ? std::min(g[1].blend[i], g[1].kept[i]) : 0;
+                    const int ebx = j > 0 ? std::min(g[2].blend[j], g[2].kept[j]) : 0;
+                    const int np = tb::tile_pieces(ndim, g[0].kept[k], g[1].kept[i], g[2].kept[j], ebt, eby, ebx,
+                                                   vec, r);
+                    max_p = std::max(max_p, np);
+                    total += np;
+                }
+        total *= planes;
+    };
+    int max_pieces = 0;
+    int64_t total_pieces = 0;
+    count(rpt, max_pieces, total_pieces);
+    if (TB_STITCH_WAVE_FIT && ndim == 2) {
+        int sms = 0;
+        if (device_sms(&sms) == TB_OK && sms > 0) {
+            const int64_t wave = (int64_t)sms * TB_STITCH_WAVE_CTAS;
+            if (total_pieces < 3 * wave) {
+                // the rows per thread whose piece count comes closest to one
+                // wave without passing it
+                int best = rpt;
+                int64_t best_n = total_pieces <= wave ? total_pieces : -1;
+                for (int r = 8; r <= 40; r += 2) {
+                    int mp = 0;
+                    int64_t n = 0;
+                    count(r, mp, n);
+                    if (n <= wave && n > best_n) {
+                        best = r;
+                        best_n = n;
+                    }
+                }
+                if (best != rpt) {
+                    rpt = best;
+                    count(rpt, max_pieces, total_pieces);
+                }
             }
+        }
+    }
+    int max_ebx = 0, max_eby = 0;
+    for (int j = 1; j < g[2].n; ++j) max_ebx = std::max(max_ebx, std::min(g[2].blend[j], g[2].kept[j]));
+    for (int i = 1; i < g[1].n; ++i) max_eby = std::max(max_eby, std::min(g[1].blend[i], g[1].kept[i]));
     prm.rows_per_thread = rpt;
     if (max_pieces == 0) return TB_OK;
     if ((int64_t)ntiles * planes > 2147483647LL || max_pieces > 65535) return TB_ERR_UNSUPPORTED;
@@ -624,6 +676,11 @@ tb_status gn_parts(int32_t P, int64_t N, int64_t C, const int64_t* spatial, int3
     want = std::min<int64_t>(want, bytes / 16384);
     int k = 1;
     while (k * 2 <= TB_GN_PARTS && k * 2 <= want) k *= 2;
+    if (TB_GN_WAVE_FIT && units > 0) {
+        // as many parts as keep the grid within one wave, each >= 16 KB
+        const int64_t fit = std::min<int64_t>((int64_t)TB_GN_WAVE_CTAS * sms / units, bytes / 16384);
+        k = (int)std::max<int64_t>(1, std::min<int64_t>(TB_GN_PARTS, fit));
+    }
     if (TB_GN_FORCE_PARTS > 0) k = TB_GN_FORCE_PARTS;
     *parts = k;
     return TB_OK;
