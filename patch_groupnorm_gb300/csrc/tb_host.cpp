@@ -1162,6 +1162,20 @@ TB_API tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int6
     prm.out = out;
     prm.status = debug_status();
     prm.planes = planes;
+    // rectangles grouped by cover counts, so CTAs dispatched together mostly
+    // run the same code path
+    for (int sy = 0; sy < prm.ay.nseg; ++sy) {
+        const int c = prm.ay.seg_n[sy] - 1;
+        prm.yseg[c][prm.ycnt[c]++] = (int16_t)sy;
+    }
+    for (int sx = 0; sx < prm.ax.nseg; ++sx) {
+        const int c = prm.ax.seg_n[sx] - 1;
+        prm.xseg[c][prm.xcnt[c]++] = (int16_t)sx;
+    }
+    prm.group_start[0] = 0;
+    for (int g = 0; g < tb::RAMP_MAXCOVER * tb::RAMP_MAXCOVER; ++g)
+        prm.group_start[g + 1] =
+            prm.group_start[g] + prm.ycnt[g / tb::RAMP_MAXCOVER] * prm.xcnt[g % tb::RAMP_MAXCOVER];
     // A piece is a run of rows of one rectangle with every plane's rows laid
     // end to end, so rectangles a few rows high still fill whole CTAs.  Rows
     // per thread start at TB_RAMP_MAX_ROWS_PER_THREAD and halve (down to 2)

@@ -274,6 +274,13 @@ struct RampParams {
     int64_t planes;
     RampAxisK ay, ax;
     int32_t rows_per_piece[RAMP_MAXSEG];  // flattened (plane, row) rows per piece, by width segment
+    // Rectangles in grid order grouped by (height cover, width cover): the
+    // segments of each axis listed by cover count, and where each of the 9
+    // groups starts among the grid's first coordinate.
+    int16_t yseg[RAMP_MAXCOVER][RAMP_MAXSEG];
+    int16_t xseg[RAMP_MAXCOVER][RAMP_MAXSEG];
+    int32_t ycnt[RAMP_MAXCOVER], xcnt[RAMP_MAXCOVER];
+    int32_t group_start[RAMP_MAXCOVER * RAMP_MAXCOVER + 1];
 };
 static_assert(sizeof(RampParams) <= 32000, "kernel parameter block too large");
 

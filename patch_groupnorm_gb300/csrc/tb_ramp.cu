@@ -305,35 +305,322 @@ __device__ __forceinline__ void run_rect(const RampParams& p, int sy, int sx, in
     }
 }
 
+// ---------------------------------------------------------------------------
+// 16-byte path: weights precomputed per CTA, lane pairs in packed fp32
+// ---------------------------------------------------------------------------
+
+// Rows of a rectangle whose normalised height weights one CTA tabulates in
+// shared memory (longer multi-cover rectangles compute them per row).
+constexpr int RAMP_WY_CAP = 512;
+
+using u64 = unsigned long long;
+__device__ __forceinline__ u64 pk2(float lo, float hi) {
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk2(u64 v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+    u64 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+    u64 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// A 16-byte chunk as fp32 lane pairs (element 2w in the low half).
+template <int DT>
+__device__ __forceinline__ void chunk_pairs(const uint4& v, u64 (&x)[RElt<DT>::BYTES == 4 ? 2 : 4]) {
+    if constexpr (RElt<DT>::BYTES == 4) {
+        x[0] = pk2(__uint_as_float(v.x), __uint_as_float(v.y));
+        x[1] = pk2(__uint_as_float(v.z), __uint_as_float(v.w));
+    } else {
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float lo, hi;
+            RElt<DT>::unpack2(wd[q], lo, hi);
+            x[q] = pk2(lo, hi);
+        }
+    }
+}
+template <int DT>
+__device__ __forceinline__ uint4 pairs_chunk(const u64 (&a)[RElt<DT>::BYTES == 4 ? 2 : 4]) {
+    if constexpr (RElt<DT>::BYTES == 4) {
+        float f0, f1, f2, f3;
+        upk2(a[0], f0, f1);
+        upk2(a[1], f2, f3);
+        return make_uint4(__float_as_uint(f0), __float_as_uint(f1), __float_as_uint(f2), __float_as_uint(f3));
+    } else {
+        uint32_t wd[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float lo, hi;
+            upk2(a[q], lo, hi);
+            wd[q] = RElt<DT>::pack2(lo, hi);
+        }
+        return make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    }
+}
+
+// Position of a row in a rectangle's flattened (plane, row) space, with the
+// byte offset of that row in a source tile and in the output, stepped `bdy`
+// rows at a time with additions only.
+struct RowCursor {
+    int plane, yl;
+    int64_t src, dst;
+};
+
+template <int CY, int CX, int DT>
+__device__ __forceinline__ void run_rect_vec(const RampParams& p, int sy, int sx, int fbeg, int fend,
+                                             uint32_t s_ring, const float* s_wy, bool wy_table) {
+    constexpr int VEC = 16 / RElt<DT>::BYTES;
+    constexpr int NP = RElt<DT>::BYTES == 4 ? 2 : 4;  // lane pairs per chunk
+    constexpr int NU = CY * CX;
+    constexpr int S = RAMP_SLOTS / NU >= 2 ? RAMP_SLOTS / NU : 1;
+    const RampAxisK& AY = p.ay;
+    const RampAxisK& AX = p.ax;
+    const int width = AX.seg_len[sx] / VEC;  // chunks
+    const int bdx = width < RAMP_BLOCK ? width : RAMP_BLOCK;
+    const int bdy = RAMP_BLOCK / bdx;
+    const int tx = threadIdx.x % bdx;
+    const int ty = threadIdx.x / bdx;
+    if (ty >= bdy) return;
+    const uint32_t slot_stride = RAMP_BLOCK * 16u;
+    const uint32_t my_slot = s_ring + threadIdx.x * 16u;
+    const int y0 = AY.seg_start[sy];
+    const int len = AY.seg_len[sy];
+    const int32_t pitch = AX.T * RElt<DT>::BYTES;
+    const int64_t tplane = (int64_t)AY.T * AX.T * RElt<DT>::BYTES;
+    const int32_t opitch = AX.out * RElt<DT>::BYTES;
+    const int64_t oplane = (int64_t)AY.out * AX.out * RElt<DT>::BYTES;
+    const int64_t tbytes = p.planes * tplane;                        // bounds-checked build
+    const int64_t obytes = p.planes * oplane;
+    const int sq = bdy / len, sr = bdy % len;
+    const int64_t src_step = sq * tplane + (int64_t)sr * pitch, src_wrap = tplane - (int64_t)len * pitch;
+    const int64_t dst_step = sq * oplane + (int64_t)sr * opitch, dst_wrap = oplane - (int64_t)len * opitch;
+    auto advance = [&](RowCursor& c) {
+        c.plane += sq;
+        c.yl += sr;
+        c.src += src_step;
+        c.dst += dst_step;
+        if (c.yl >= len) {
+            c.yl -= len;
+            ++c.plane;
+            c.src += src_wrap;
+            c.dst += dst_wrap;
+        }
+    };
+    const int r0 = fbeg + ty;
+    const int nrows = r0 < fend ? (fend - r0 + bdy - 1) / bdy : 0;
+    RowCursor first;
+    first.plane = r0 / len;
+    first.yl = r0 - first.plane * len;
+    first.src = first.plane * tplane + (int64_t)first.yl * pitch;
+    first.dst = first.plane * oplane + (int64_t)first.yl * opitch;
+
+    for (int c = tx; c < width; c += bdx) {
+        const int x0 = AX.seg_start[sx] + c * VEC;
+        // normalised width weights of this chunk's lanes, as lane pairs
+        u64 wxp[CX][NP];
+        if constexpr (CX > 1) {
+            float wx[CX][VEC];
+#pragma unroll
+            for (int l = 0; l < VEC; ++l) {
+                float sum = 0.f;
+#pragma unroll
+                for (int b = 0; b < CX; ++b) {
+                    wx[b][l] = axis_w<CX>(AX, sx, b, x0 + l);
+                    sum += wx[b][l];
+                }
+                const float inv = 1.0f / sum;
+#pragma unroll
+                for (int b = 0; b < CX; ++b) wx[b][l] *= inv;
+            }
+#pragma unroll
+            for (int b = 0; b < CX; ++b)
+#pragma unroll
+                for (int w = 0; w < NP; ++w) wxp[b][w] = pk2(wx[b][2 * w], wx[b][2 * w + 1]);
+        }
+        const char* src[NU];
+        const char* tbase[NU];
+#pragma unroll
+        for (int a = 0; a < CY; ++a)
+#pragma unroll
+            for (int b = 0; b < CX; ++b) {
+                const int ti = AY.seg_tile[sy][a], tj = AX.seg_tile[sx][b];
+                index_ok(ti >= 0 && ti < AY.n && tj >= 0 && tj < AX.n, p.status);
+                tbase[a * CX + b] = reinterpret_cast<const char*>(p.tiles[ti * AX.n + tj]);
+                src[a * CX + b] = tbase[a * CX + b] +
+                                  ((int64_t)(y0 - AY.org[ti]) * AX.T + (x0 - AX.org[tj])) * RElt<DT>::BYTES;
+            }
+        char* const dst = reinterpret_cast<char*>(p.out) + ((int64_t)y0 * AX.out + x0) * RElt<DT>::BYTES;
+
+        RowCursor ahead = first;  // the next row to fetch
+        auto issue = [&](int m) {
+            const uint32_t st = my_slot + (uint32_t)((m % S) * NU) * slot_stride;
+#pragma unroll
+            for (int n = 0; n < NU; ++n)
+                if (in_bounds(src[n] + ahead.src, 16, tbase[n], tbytes, p.status))
+                    cp_async16(st + (uint32_t)n * slot_stride, src[n] + ahead.src);
+            advance(ahead);
+        };
+#pragma unroll
+        for (int m = 0; m < S - 1; ++m) {
+            if (m < nrows) issue(m);
+            cp_async_commit();
+        }
+        RowCursor at = first;
+        for (int m = 0; m < nrows; ++m) {
+            if (m + S - 1 < nrows) issue(m + S - 1);
+            cp_async_commit();
+            cp_async_wait<S - 1>();
+            const uint32_t st = my_slot + (uint32_t)((m % S) * NU) * slot_stride;
+            uint4 o;
+            if constexpr (NU == 1) {
+                o = lds16(st);  // one tile: its normalised weight is exactly 1
+            } else {
+                float wy[CY];
+                if constexpr (CY > 1) {
+                    if (wy_table) {
+#pragma unroll
+                        for (int a = 0; a < CY; ++a) wy[a] = s_wy[at.yl * CY + a];
+                    } else {
+                        float sum = 0.f;
+#pragma unroll
+                        for (int a = 0; a < CY; ++a) {
+                            wy[a] = axis_w<CY>(AY, sy, a, y0 + at.yl);
+                            sum += wy[a];
+                        }
+                        const float inv = 1.0f / sum;
+#pragma unroll
+                        for (int a = 0; a < CY; ++a) wy[a] *= inv;
+                    }
+                }
+                // sum over a of wy[a] * (sum over b of wx[b] * x_ab), lane pairs
+                u64 acc[NP];
+#pragma unroll
+                for (int a = 0; a < CY; ++a) {
+                    u64 inner[NP];
+#pragma unroll
+                    for (int b = 0; b < CX; ++b) {
+                        u64 x[NP];
+                        chunk_pairs<DT>(lds16(st + (uint32_t)(a * CX + b) * slot_stride), x);
+#pragma unroll
+                        for (int w = 0; w < NP; ++w) {
+                            if constexpr (CX == 1) inner[w] = x[w];
+                            else inner[w] = b == 0 ? mul2(x[w], wxp[0][w]) : fma2(x[w], wxp[b][w], inner[w]);
+                        }
+                    }
+                    if constexpr (CY == 1) {
+#pragma unroll
+                        for (int w = 0; w < NP; ++w) acc[w] = inner[w];
+                    } else {
+                        const u64 wyp = pk2(wy[a], wy[a]);
+#pragma unroll
+                        for (int w = 0; w < NP; ++w) acc[w] = a == 0 ? mul2(inner[w], wyp) : fma2(inner[w], wyp, acc[w]);
+                    }
+                }
+                o = pairs_chunk<DT>(acc);
+            }
+            char* const ot = dst + at.dst;
+            if (in_bounds(ot, 16, p.out, obytes, p.status)) __stcs(reinterpret_cast<uint4*>(ot), o);
+            advance(at);
+        }
+        cp_async_wait<0>();
+    }
+}
+
+#ifndef TB_RAMP_GROUP_ORDER
+#define TB_RAMP_GROUP_ORDER 1
+#endif
+
 template <int DT, int VEC>
 __global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_constant__ RampParams p) {
     extern __shared__ __align__(16) unsigned char s_ring[];
+    __shared__ float s_wy[RAMP_WY_CAP * RAMP_MAXCOVER];
     // A piece is a run of rows of one rectangle, in the rectangle's (plane,
-    // row) space flattened over all planes.  blockIdx.x is the rectangle
-    // (row-major over (sy, sx)) and blockIdx.y the piece index, so the CTAs
-    // launched first cover every rectangle, i.e. whole rows of the canvas;
-    // rectangles with fewer pieces leave their trailing CTAs empty.
-    const int sy = (int)blockIdx.x / p.ax.nseg;
-    const int sx = (int)blockIdx.x % p.ax.nseg;
+    // row) space flattened over all planes.  blockIdx.y is the piece index and
+    // blockIdx.x the rectangle, so the CTAs launched first cover every
+    // rectangle, i.e. whole rows of the canvas; rectangles with fewer pieces
+    // leave their trailing CTAs empty.  The rectangles are numbered group by
+    // group of equal (height cover, width cover), so that CTAs dispatched
+    // together mostly run one code path (fewer instruction-cache misses).
+    int sy, sx;
+#if TB_RAMP_GROUP_ORDER
+    {
+        const int bx = (int)blockIdx.x;
+        int g = 0;
+        while (g + 1 < RAMP_MAXCOVER * RAMP_MAXCOVER && p.group_start[g + 1] <= bx) ++g;
+        const int gy = g / RAMP_MAXCOVER, gx = g - gy * RAMP_MAXCOVER;
+        const int idx = bx - p.group_start[g];
+        const int iy = idx / p.xcnt[gx];
+        sy = p.yseg[gy][iy];
+        sx = p.xseg[gx][idx - iy * p.xcnt[gx]];
+    }
+#else
+    sy = (int)blockIdx.x / p.ax.nseg;
+    sx = (int)blockIdx.x % p.ax.nseg;
+#endif
     const int rem = (int)blockIdx.y;
     const int flat = (int)p.planes * p.ay.seg_len[sy];
     const int fbeg = rem * p.rows_per_piece[sx];
     if (fbeg >= flat) return;
     const int fend = min(flat, fbeg + p.rows_per_piece[sx]);
+    const int cy = p.ay.seg_n[sy], cx = p.ax.seg_n[sx];
+    // the rectangle's normalised height weights (parameters only)
+    const int len = p.ay.seg_len[sy];
+    const bool wy_table = cy > 1 && len <= RAMP_WY_CAP;
+    if constexpr (VEC * RElt<DT>::BYTES == 16) {
+        if (wy_table) {
+            const int y0 = p.ay.seg_start[sy];
+            for (int yl = threadIdx.x; yl < len; yl += RAMP_BLOCK) {
+                float w[RAMP_MAXCOVER], sum = 0.f;
+                for (int a = 0; a < cy; ++a) {
+                    w[a] = axis_w<1>(p.ay, sy, a, y0 + yl);
+                    sum += w[a];
+                }
+                const float inv = 1.0f / sum;
+                for (int a = 0; a < cy; ++a) s_wy[yl * cy + a] = w[a] * inv;
+            }
+            __syncthreads();
+        }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(s_ring);
-    const int cy = p.ay.seg_n[sy], cx = p.ax.seg_n[sx];
-    switch (cy * 4 + cx) {
-        case 5: run_rect<1, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-        case 6: run_rect<1, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-        case 7: run_rect<1, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-        case 9: run_rect<2, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-        case 10: run_rect<2, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-        case 11: run_rect<2, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-        case 13: run_rect<3, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-        case 14: run_rect<3, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-        case 15: run_rect<3, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-        default: break;
+    if constexpr (VEC * RElt<DT>::BYTES == 16) {
+#define TB_RECT(CY_, CX_) run_rect_vec<CY_, CX_, DT>(p, sy, sx, fbeg, fend, ring, s_wy, wy_table)
+        switch (cy * 4 + cx) {
+            case 5: TB_RECT(1, 1); break;
+            case 6: TB_RECT(1, 2); break;
+            case 7: TB_RECT(1, 3); break;
+            case 9: TB_RECT(2, 1); break;
+            case 10: TB_RECT(2, 2); break;
+            case 11: TB_RECT(2, 3); break;
+            case 13: TB_RECT(3, 1); break;
+            case 14: TB_RECT(3, 2); break;
+            case 15: TB_RECT(3, 3); break;
+            default: break;
+        }
+#undef TB_RECT
+    } else {
+        switch (cy * 4 + cx) {
+            case 5: run_rect<1, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+            case 6: run_rect<1, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+            case 7: run_rect<1, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+            case 9: run_rect<2, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+            case 10: run_rect<2, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+            case 11: run_rect<2, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+            case 13: run_rect<3, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+            case 14: run_rect<3, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+            case 15: run_rect<3, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
+            default: break;
+        }
     }
 }
 
