@@ -504,6 +504,30 @@ def per_kernel(torch, tb, W, dev, peak, reps, only=None):
                   "stitch3d", name)
         del sets
         torch.cuda.empty_cache()
+    for name in ("image_2048_bf16", "video_49x480x832_bf16"):
+        # the band the first of two ranks packs for the second in a
+        # row-sharded stitch: read once, written once
+        if not wanted(name, "halo_pack"):
+            continue
+        w = W.STITCH[name]
+        axes = [tb.Axis(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in w.axes]
+        lays = [tb.tb_axis_layout(a) for a in axes]
+        tiles = W.make_stitch_tiles(w, [list(zip(l.origins, l.extents)) for l in lays], [l.out_extent for l in lays])
+        at, ay, ax = (None, axes[0], axes[1]) if w.ndim == 2 else axes
+        lay = tb.tb_stitch_shard_layout(at, ay, ax, w.B, w.C, 2, 0)
+        row = lay.row_end - 1
+        tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+        esize = 4 if w.dtype == "f32" else 2
+        nbytes = 2 * lay.send_elems * esize
+        ns = nsets_for(nbytes)
+        sets = []
+        for _ in range(ns):
+            rt = [t.to(dev) for t in tiles[row]] if w.ndim == 2 else [[t.to(dev) for t in pl[row]] for pl in tiles]
+            sets.append((rt, torch.empty(lay.send_elems, dtype=tdt, device=dev)))
+        timed(lambda q: tb.tb_stitch_halo_pack(sets[q][0], at, ay, ax, row, sets[q][1]), ns, nbytes, "halo_pack",
+              name)
+        del sets
+        torch.cuda.empty_cache()
     for name, w in W.RAMP.items():
         if not wanted(name, "stitch2d_ramp"):
             continue
@@ -605,6 +629,22 @@ def run_profile_target(args):
         tdt = dt[0][0].dtype
         out = torch.empty((w.B, w.C, ay.out_extent, ax.out_extent), dtype=tdt, device=dev)
         launch = lambda: tb.tb_stitch2d_ramp(dt, ay, ax, out)
+    elif kernel == "halo_pack":
+        # the band the first of two ranks sends in a row-sharded stitch
+        w = W.STITCH[name]
+        axes = [tb.Axis(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in w.axes]
+        lays = [tb.tb_axis_layout(a) for a in axes]
+        tiles = W.make_stitch_tiles(w, [list(zip(l.origins, l.extents)) for l in lays], [l.out_extent for l in lays])
+        at, ay, ax = (None, axes[0], axes[1]) if w.ndim == 2 else axes
+        lay = tb.tb_stitch_shard_layout(at, ay, ax, w.B, w.C, 2, 0)
+        row = lay.row_end - 1
+        tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+        if w.ndim == 2:
+            rt = [t.to(dev) for t in tiles[row]]
+        else:
+            rt = [[t.to(dev) for t in pl[row]] for pl in tiles]
+        band = torch.empty(lay.send_elems, dtype=tdt, device=dev)
+        launch = lambda: tb.tb_stitch_halo_pack(rt, at, ay, ax, row, band)
     elif kernel == "copy":
         # a plain copy of WORKLOAD megabytes (half read, half written) through
         # the library's copy kernel: the single-launch reference for a
@@ -764,7 +804,7 @@ def main():
                     help="comma-separated workloads or kernel names: print only their per-kernel timings")
     ap.add_argument("--profile", default=None,
                     help="KERNEL:WORKLOAD (stitch2d|stitch3d|stitch2d_ramp|gn_stats|gn_apply|patchify|"
-                         "gather_patches, or copy:MEGABYTES): plain launches for ncu")
+                         "gather_patches|halo_pack, or copy:MEGABYTES): plain launches for ncu")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -13,7 +13,7 @@
 // halo_pack_kernel gathers those rows of every tile of one tile row into one
 // dense buffer, so the exchange is a single message per rank boundary.  It
 // moves chunks of `VB` bytes (the widest power of two up to 16 dividing every
-// row, offset and address); CTA (b, q) copies the b-th range of band q.
+// row, offset and address).
 #include "tb_internal.h"
 
 namespace tb {
@@ -42,28 +42,49 @@ struct Vec<1> {
     using T = uint8_t;
 };
 
+// CTA (b, q) copies band rows [b * per_cta, (b + 1) * per_cta) of band q;
+// a band row is one of the `e` rows of one (plane, frame), `width` chunks
+// long at the same place in the source tile and in the band.  Threads lie
+// across a row (bdx of them) and over `HALO_BLOCK / bdx` rows at a time, so
+// each thread divides once per row, and issues HALO_INFLIGHT loads before
+// its stores.
+constexpr int HALO_INFLIGHT = 4;
+
 template <int VB>
 __global__ void __launch_bounds__(HALO_BLOCK) halo_pack_kernel(const __grid_constant__ HaloPackParams p) {
     using T = typename Vec<VB>::T;
     const int q = blockIdx.y;
-    const int64_t n = p.n[q];
-    const int64_t c0 = (int64_t)blockIdx.x * p.per_cta;
-    const int64_t c1 = c0 + p.per_cta < n ? c0 + p.per_cta : n;
-    const uint64_t w = (uint64_t)p.width[q];
-    const uint64_t e = (uint64_t)p.e;
-    const uint64_t L = (uint64_t)p.rows[q];
+    const uint32_t w = (uint32_t)p.width[q];
+    const uint32_t e = (uint32_t)p.e;
+    const uint32_t L = (uint32_t)p.rows[q];
+    const int64_t nrows = p.n[q] / w;                      // band rows of band q
+    const int64_t r0 = (int64_t)blockIdx.x * p.per_cta;
+    const int64_t r1 = r0 + p.per_cta < nrows ? r0 + p.per_cta : nrows;
+    const uint32_t bdx = w < (uint32_t)HALO_BLOCK ? w : (uint32_t)HALO_BLOCK;
+    const uint32_t bdy = HALO_BLOCK / bdx;
+    const uint32_t tx = threadIdx.x % bdx, ty = threadIdx.x / bdx;
+    if (ty >= bdy) return;
     const T* src = reinterpret_cast<const T*>(p.src[q]);
     T* dst = reinterpret_cast<T*>(p.dst) + p.dst_off[q];
-    const int64_t src_bytes = n / (int64_t)e * (int64_t)L * VB;  // bounds-checked build
-    for (int64_t c = c0 + threadIdx.x; c < c1; c += HALO_BLOCK) {
-        const uint64_t r = (uint64_t)c / w;      // (plane, frame, band row), flattened
-        const uint64_t x = (uint64_t)c - r * w;
-        const uint64_t fp = r / e;               // (plane, frame)
-        const uint64_t row = r - fp * e;
-        const T* at = src + (fp * L + (L - e + row)) * w + x;
-        if (in_bounds(at, VB, src, src_bytes, p.status) &&
-            in_bounds(dst + c, VB, p.dst, p.dst_total * VB, p.status))
-            dst[c] = __ldcs(at);
+    const int64_t src_bytes = nrows / e * (int64_t)L * w * VB;  // bounds-checked build
+    for (int64_t r = r0 + ty; r < r1; r += bdy) {
+        const int64_t fp = r / e;                            // (plane, frame)
+        const int64_t row = r - fp * e;
+        const T* srow = src + ((uint64_t)fp * L + (L - e + row)) * w;
+        T* drow = dst + (uint64_t)r * w;
+        for (uint32_t x0 = tx; x0 < w; x0 += bdx * HALO_INFLIGHT) {
+            T v[HALO_INFLIGHT];
+#pragma unroll
+            for (int u = 0; u < HALO_INFLIGHT; ++u) {
+                const uint32_t x = x0 + u * bdx;
+                if (x < w && in_bounds(srow + x, VB, src, src_bytes, p.status)) v[u] = __ldcs(srow + x);
+            }
+#pragma unroll
+            for (int u = 0; u < HALO_INFLIGHT; ++u) {
+                const uint32_t x = x0 + u * bdx;
+                if (x < w && in_bounds(drow + x, VB, p.dst, p.dst_total * VB, p.status)) __stcs(drow + x, v[u]);
+            }
+        }
     }
 }
 
