@@ -1065,15 +1065,10 @@ TB_API tb_status tb_stitch_halo_pack(const void* const* tiles, tb_dtype dtype, i
             most = std::max(most, prm.n[q]);
         }
     prm.dst_total = off;
-    // band rows per CTA: about 32 KB each
-    int64_t max_w = 1;
-    for (int64_t q = 0; q < ntiles; ++q) max_w = std::max<int64_t>(max_w, prm.width[q]);
-    const int64_t cta = std::max<int64_t>(1, 32768 / (max_w * vb));
+    // chunks per CTA: 8 rounds of 256 threads, 32 KB of 16-byte chunks
+    const int64_t cta = (int64_t)tb::HALO_BLOCK * 8;
     prm.per_cta = cta;
-    int64_t most_rows = 0;
-    for (int64_t q = 0; q < ntiles; ++q) most_rows = std::max<int64_t>(most_rows, prm.n[q] / prm.width[q]);
-    (void)most;
-    const int64_t ranges = (most_rows + cta - 1) / cta;
+    const int64_t ranges = (most + cta - 1) / cta;
     if (ranges > 2147483647LL) return TB_ERR_UNSUPPORTED;
     cudaError_t e2 = tb::launch_halo_pack(prm, vb, ranges, reinterpret_cast<cudaStream_t>(stream));
     if (e2 != cudaSuccess) return cuda_fail(e2);

@@ -339,7 +339,7 @@ struct HaloPackParams {
     int32_t rows[HALO_MAXT];       // rows per frame of source tile q
     int32_t width[HALO_MAXT];      // chunks per row of source tile q
     void* dst;
-    int64_t per_cta;               // band rows one CTA copies
+    int64_t per_cta;               // chunks one CTA copies
     int64_t dst_total;             // chunks of the whole halo buffer
     uint32_t* status;              // device status word (bounds-checked build), or null
     int32_t e;                     // band rows

@@ -42,49 +42,61 @@ struct Vec<1> {
     using T = uint8_t;
 };
 
-// CTA (b, q) copies band rows [b * per_cta, (b + 1) * per_cta) of band q;
-// a band row is one of the `e` rows of one (plane, frame), `width` chunks
-// long at the same place in the source tile and in the band.  Threads lie
-// across a row (bdx of them) and over `HALO_BLOCK / bdx` rows at a time, so
-// each thread divides once per row, and issues HALO_INFLIGHT loads before
-// its stores.
-constexpr int HALO_INFLIGHT = 4;
+// CTA (b, q) copies chunks [b * per_cta, (b + 1) * per_cta) of band q, in
+// the band's own order ((plane, frame), band row, column).  A thread divides
+// twice to find its first chunk's (plane and frame, band row, column), then
+// steps HALO_BLOCK chunks at a time by additions, and keeps HALO_INFLIGHT
+// loads in flight before it stores them.
+constexpr int HALO_INFLIGHT = 8;
 
 template <int VB>
 __global__ void __launch_bounds__(HALO_BLOCK) halo_pack_kernel(const __grid_constant__ HaloPackParams p) {
     using T = typename Vec<VB>::T;
     const int q = blockIdx.y;
+    const int64_t n = p.n[q];
+    int64_t c = (int64_t)blockIdx.x * p.per_cta + threadIdx.x;
+    const int64_t c1 = (int64_t)blockIdx.x * p.per_cta + p.per_cta < n ? (int64_t)blockIdx.x * p.per_cta + p.per_cta : n;
+    if (c >= c1) return;
     const uint32_t w = (uint32_t)p.width[q];
     const uint32_t e = (uint32_t)p.e;
     const uint32_t L = (uint32_t)p.rows[q];
-    const int64_t nrows = p.n[q] / w;                      // band rows of band q
-    const int64_t r0 = (int64_t)blockIdx.x * p.per_cta;
-    const int64_t r1 = r0 + p.per_cta < nrows ? r0 + p.per_cta : nrows;
-    const uint32_t bdx = w < (uint32_t)HALO_BLOCK ? w : (uint32_t)HALO_BLOCK;
-    const uint32_t bdy = HALO_BLOCK / bdx;
-    const uint32_t tx = threadIdx.x % bdx, ty = threadIdx.x / bdx;
-    if (ty >= bdy) return;
+    const uint64_t r = (uint64_t)c / w;            // (plane, frame, band row)
+    uint32_t x = (uint32_t)((uint64_t)c - r * w);
+    uint64_t fp = r / e;                            // (plane, frame)
+    uint32_t brow = (uint32_t)(r - fp * e);
+    const uint32_t rstep = HALO_BLOCK / w, xstep = HALO_BLOCK % w;
     const T* src = reinterpret_cast<const T*>(p.src[q]);
     T* dst = reinterpret_cast<T*>(p.dst) + p.dst_off[q];
-    const int64_t src_bytes = nrows / e * (int64_t)L * w * VB;  // bounds-checked build
-    for (int64_t r = r0 + ty; r < r1; r += bdy) {
-        const int64_t fp = r / e;                            // (plane, frame)
-        const int64_t row = r - fp * e;
-        const T* srow = src + ((uint64_t)fp * L + (L - e + row)) * w;
-        T* drow = dst + (uint64_t)r * w;
-        for (uint32_t x0 = tx; x0 < w; x0 += bdx * HALO_INFLIGHT) {
-            T v[HALO_INFLIGHT];
+    const int64_t src_bytes = n / (int64_t)(e * w) * (int64_t)L * w * VB;  // bounds-checked build
+    while (c < c1) {
+        T v[HALO_INFLIGHT];
+        int64_t at[HALO_INFLIGHT];
 #pragma unroll
-            for (int u = 0; u < HALO_INFLIGHT; ++u) {
-                const uint32_t x = x0 + u * bdx;
-                if (x < w && in_bounds(srow + x, VB, src, src_bytes, p.status)) v[u] = __ldcs(srow + x);
+        for (int u = 0; u < HALO_INFLIGHT; ++u) {
+            at[u] = -1;
+            if (c < c1) {
+                const T* s = src + (fp * L + (L - e + brow)) * w + x;
+                if (in_bounds(s, VB, src, src_bytes, p.status)) {
+                    v[u] = __ldcs(s);
+                    at[u] = c;
+                }
             }
-#pragma unroll
-            for (int u = 0; u < HALO_INFLIGHT; ++u) {
-                const uint32_t x = x0 + u * bdx;
-                if (x < w && in_bounds(drow + x, VB, p.dst, p.dst_total * VB, p.status)) __stcs(drow + x, v[u]);
+            c += HALO_BLOCK;
+            x += xstep;
+            uint32_t dr = rstep;
+            if (x >= w) {
+                x -= w;
+                ++dr;
+            }
+            brow += dr;
+            while (brow >= e) {
+                brow -= e;
+                ++fp;
             }
         }
+#pragma unroll
+        for (int u = 0; u < HALO_INFLIGHT; ++u)
+            if (at[u] >= 0 && in_bounds(dst + at[u], VB, p.dst, p.dst_total * VB, p.status)) __stcs(dst + at[u], v[u]);
     }
 }
 

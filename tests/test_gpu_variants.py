@@ -12,7 +12,10 @@ through TILEBLEND_LIB):
   test);
 * the TMA build (TB_STITCH_TMA=1): the stitch stages each piece's source
   rectangles with tensor copies instead of the per-thread cp.async rings; it
-  must be bit-exact on every stitch and shard test as well.
+  must be bit-exact on every stitch and shard test as well;
+* a GroupNorm build that cuts every statistics unit into 3 parts
+  (TB_GN_FORCE_PARTS=3): records 3 to 7 of each unit are then empty and
+  filled by the part CTAs in turn; the GroupNorm tests must still pass.
 """
 import os
 import subprocess
@@ -26,6 +29,7 @@ VARIANTS = {
     "debug_bounds": (["TB_DEBUG_BOUNDS=1"], ["tests/test_gpu_patchify.py", "tests/test_gpu_ramp.py",
                                               "tests/test_gpu_shard.py", "tests/test_gpu_stitch.py"]),
     "tma": (["TB_STITCH_TMA=1"], ["tests/test_gpu_shard.py", "tests/test_gpu_stitch.py"]),
+    "gn_parts3": (["TB_GN_FORCE_PARTS=3"], ["tests/test_gpu_groupnorm.py", "tests/test_zz_no_alloc.py"]),
 }
 
 
