@@ -25,7 +25,10 @@ PR #14):
   (``tb_patch_gn_apply_gathered``).
 
 ``exchange_halo`` and ``gather_partials`` carry no arithmetic and work on any
-backend, so their rank logic is tested on CPU ranks over gloo.
+backend.  The entry points take the library binding as ``lib`` (the
+default, ``tileblend``, is the only one the product uses); tests on CPU
+ranks pass an object with the same calls backed by the CPU oracle, to run
+this module's rank logic over gloo.
 """
 from typing import List, Optional, Sequence
 
@@ -62,7 +65,7 @@ def exchange_halo(send: Optional[torch.Tensor], recv: Optional[torch.Tensor], gr
 
 
 def stitch2d_row_sharded(tiles: Sequence[Sequence[torch.Tensor]], ay: tb.Axis, ax: tb.Axis, out: torch.Tensor,
-                         group=None) -> torch.Tensor:
+                         group=None, lib=tb) -> torch.Tensor:
     """This rank's rows of a row-sharded 2D stitch.
 
     ``tiles[i][j]`` are the tiles of the rank's tile rows (see
@@ -70,37 +73,37 @@ def stitch2d_row_sharded(tiles: Sequence[Sequence[torch.Tensor]], ay: tb.Axis, a
     rank's slice of the full image."""
     world, rank = _world_rank(group)
     B, C = out.shape[:2]
-    lay = tb.tb_stitch_shard_layout(None, ay, ax, B, C, world, rank)
+    lay = lib.tb_stitch_shard_layout(None, ay, ax, B, C, world, rank)
     if len(tiles) != lay.row_end - lay.row_begin:
         raise ValueError("rank %d holds tile rows [%d, %d)" % (rank, lay.row_begin, lay.row_end))
     send = recv = None
     if lay.send_elems:
         send = torch.empty(lay.send_elems, dtype=out.dtype, device=out.device)
-        tb.tb_stitch_halo_pack(tiles[-1], None, ay, ax, lay.row_end - 1, send)
+        lib.tb_stitch_halo_pack(tiles[-1], None, ay, ax, lay.row_end - 1, send)
     if lay.halo_elems:
         recv = torch.empty(lay.halo_elems, dtype=out.dtype, device=out.device)
     exchange_halo(send, recv, group)
-    return tb.tb_stitch2d_shard(tiles, recv, ay, ax, lay.row_begin, lay.row_end, out)
+    return lib.tb_stitch2d_shard(tiles, recv, ay, ax, lay.row_begin, lay.row_end, out)
 
 
 def stitch3d_row_sharded(tiles, at: tb.Axis, ay: tb.Axis, ax: tb.Axis, out: torch.Tensor,
-                         group=None) -> torch.Tensor:
+                         group=None, lib=tb) -> torch.Tensor:
     """This rank's rows of a video stitch sharded along the height:
     ``tiles[k][i][j]`` over all frame tiles k and the rank's tile rows i;
     ``out`` is [B, C, T, out_rows, W]."""
     world, rank = _world_rank(group)
     B, C = out.shape[:2]
-    lay = tb.tb_stitch_shard_layout(at, ay, ax, B, C, world, rank)
+    lay = lib.tb_stitch_shard_layout(at, ay, ax, B, C, world, rank)
     if any(len(per_k) != lay.row_end - lay.row_begin for per_k in tiles):
         raise ValueError("rank %d holds tile rows [%d, %d)" % (rank, lay.row_begin, lay.row_end))
     send = recv = None
     if lay.send_elems:
         send = torch.empty(lay.send_elems, dtype=out.dtype, device=out.device)
-        tb.tb_stitch_halo_pack([per_k[-1] for per_k in tiles], at, ay, ax, lay.row_end - 1, send)
+        lib.tb_stitch_halo_pack([per_k[-1] for per_k in tiles], at, ay, ax, lay.row_end - 1, send)
     if lay.halo_elems:
         recv = torch.empty(lay.halo_elems, dtype=out.dtype, device=out.device)
     exchange_halo(send, recv, group)
-    return tb.tb_stitch3d_shard(tiles, recv, at, ay, ax, lay.row_begin, lay.row_end, out)
+    return lib.tb_stitch3d_shard(tiles, recv, at, ay, ax, lay.row_begin, lay.row_end, out)
 
 
 def gather_partials(local: torch.Tensor, group=None) -> torch.Tensor:
@@ -113,15 +116,16 @@ def gather_partials(local: torch.Tensor, group=None) -> torch.Tensor:
 
 
 def patch_group_norm_sharded(patches: Sequence[torch.Tensor], G: int, gamma, beta, eps: float, silu: bool = True,
-                             outs: Optional[Sequence[torch.Tensor]] = None, group=None) -> List[torch.Tensor]:
+                             outs: Optional[Sequence[torch.Tensor]] = None, group=None,
+                             lib=tb) -> List[torch.Tensor]:
     """GroupNorm (+ SiLU) of a tensor whose patches are spread over the ranks:
     this rank's ``patches`` come back normalised with the statistics of the
     whole tensor."""
     N = patches[0].shape[0]
     if outs is None:
         outs = [torch.empty_like(p) for p in patches]
-    local = tb.new_partials(len(patches), N, G, patches[0].device)
-    tb.tb_patch_gn_stats(patches, G, local)
+    local = lib.new_partials(len(patches), N, G, patches[0].device)
+    lib.tb_patch_gn_stats(patches, G, local)
     every = gather_partials(local, group)
-    tb.tb_patch_gn_apply_gathered(patches, outs, G, every, every.shape[0], gamma, beta, eps, silu)
+    lib.tb_patch_gn_apply_gathered(patches, outs, G, every, every.shape[0], gamma, beta, eps, silu)
     return list(outs)

@@ -256,3 +256,37 @@ def test_gathered_apply_with_empty_records_and_record_order(tbl):
         tbl.tb_patch_gn_apply_gathered([dev[p]], [outs[p]], 8, every, 4, gamma.cuda(), beta.cuda(), 1e-6, True)
     torch.cuda.synchronize()
     assert gn_violation([o.cpu() for o in outs], patches, gamma, beta, 8, 1e-6, True, "f32") <= 1.0
+
+
+def test_sharded_module_on_a_one_rank_nccl_group(tbl):
+    # the multi-rank module itself on a GPU: one rank, so the stitch needs no
+    # band and the all-gather returns the rank's own records; results equal
+    # the direct library calls bit for bit
+    import socket
+    import torch.distributed as dist
+    from patch_groupnorm_gb300 import sharded
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    dist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % port, rank=0, world_size=1)
+    try:
+        w = W.STITCH["image_2048_bf16_uniform"]
+        axes = [_axis(tbl, a) for a in w.axes]
+        lays = [tbl.tb_axis_layout(a) for a in axes]
+        tiles = W.make_stitch_tiles(w, [list(zip(l.origins, l.extents)) for l in lays],
+                                    [l.out_extent for l in lays])
+        dev = [[t.cuda() for t in row] for row in tiles]
+        shape = (w.B, w.C, lays[0].out_extent, lays[1].out_extent)
+        want = tbl.tb_stitch2d(dev, axes[0], axes[1], torch.empty(shape, dtype=torch.bfloat16, device="cuda"))
+        got = sharded.stitch2d_row_sharded(dev, axes[0], axes[1], torch.empty_like(want))
+        patches, gamma, beta = synth.groupnorm_patches(33, (1, 64, 32, 48), 2, 2, (-2.0, 2.0), "bf16")
+        dp = [p.cuda() for p in patches]
+        ref = tbl.patch_group_norm(dp, 16, gamma.cuda(), beta.cuda(), 1e-6, silu=True)
+        outs = sharded.patch_group_norm_sharded(dp, 16, gamma.cuda(), beta.cuda(), 1e-6, silu=True)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+        for o, r in zip(outs, ref):
+            assert torch.equal(o.view(torch.int16), r.view(torch.int16))
+    finally:
+        dist.destroy_process_group()

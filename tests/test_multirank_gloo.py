@@ -118,45 +118,108 @@ def _local_axis(ly, row_begin, row_end, halo_rows):
                       sum(kept))
 
 
+class _OracleLib:
+    """The calls of the library binding that patch_groupnorm_gb300.sharded
+    makes, on CPU tensors, for CPU ranks: the rank layout from the library's
+    host-only call, the stitch of a rank's grid (the received band as its
+    first tile row) and the GroupNorm records and pooling from the CPU
+    oracle and plain float64 arithmetic.  Test infrastructure only."""
+
+    def __init__(self, tb):
+        self.tb = tb
+
+    def tb_stitch_shard_layout(self, *args):
+        return self.tb.tb_stitch_shard_layout(*args)
+
+    @staticmethod
+    def _lay(a):
+        from oracle.geometry import axis_layout
+        return axis_layout(a.latent_extent, a.latent_tile, a.overlap, a.scale)
+
+    def tb_stitch_halo_pack(self, row_tiles, at, ay, ax, row, halo):
+        e = self._lay(ay).blends[row + 1]
+        flat = list(row_tiles) if at is None else [t for per_k in row_tiles for t in per_k]
+        halo.copy_(torch.cat([t[..., -e:, :].reshape(-1) for t in flat]))
+
+    def _shard(self, tiles3, halo, at, ay, ax, rb, re_, out):
+        import numpy as np
+        from oracle.stitch import stitch as oracle_stitch
+        lt = self._lay(at) if at is not None else None
+        ly, lx = self._lay(ay), self._lay(ax)
+        B, C = out.shape[:2]
+        e = ly.blends[rb] if rb > 0 else 0
+        grid3 = []
+        off = 0
+        for k, per_k in enumerate(tiles3):
+            grid = []
+            if halo is not None and e:
+                band = []
+                for w in lx.extents:
+                    shape = (B, C) + ((lt.extents[k],) if lt else ()) + (e, w)
+                    n = int(np.prod(shape))
+                    band.append(halo[off:off + n].view(shape))
+                    off += n
+                grid.append(band)
+            grid += list(per_k)
+            grid3.append([[t.numpy().view(np.uint16) for t in r] for r in grid])
+        local_y = _local_axis(ly, rb, re_, e if halo is not None else 0)
+        res = oracle_stitch(grid3, (lt, local_y, lx), "bf16") if lt else oracle_stitch(grid3[0], (local_y, lx), "bf16")
+        res = res[..., local_y.kept[0] if (halo is not None and e) else 0:, :]
+        out.copy_(torch.from_numpy(np.ascontiguousarray(res).view(np.int16)))
+        return out
+
+    def tb_stitch2d_shard(self, tiles, halo, ay, ax, rb, re_, out):
+        return self._shard([tiles], halo, None, ay, ax, rb, re_, out)
+
+    def tb_stitch3d_shard(self, tiles, halo, at, ay, ax, rb, re_, out):
+        return self._shard(tiles, halo, at, ay, ax, rb, re_, out)
+
+    def new_partials(self, P, N, G, device=None):
+        return torch.zeros((P, N, G, 8, 2), dtype=torch.int64)
+
+    def tb_patch_gn_stats(self, patches, G, partials):
+        # one record per unit: (count, mean, M2) of the patch's group elements
+        import numpy as np
+        for p, patch in enumerate(patches):
+            partials[p] = _records(patch.double().numpy(), G, 1)[0]
+
+    def tb_patch_gn_apply_gathered(self, patches, outs, G, every, R, gamma, beta, eps, silu):
+        import numpy as np
+        rec = every.numpy()
+        c = rec[..., 0].astype(np.float64)
+        mv = np.ascontiguousarray(rec[..., 1]).view(np.float32).reshape(rec.shape[:-1] + (2,)).astype(np.float64)
+        n = c.sum(axis=(0, 3))
+        mu = (c * mv[..., 0]).sum(axis=(0, 3)) / n
+        var = (mv[..., 1] + c * (mv[..., 0] - mu[None, :, :, None]) ** 2).sum(axis=(0, 3)) / n
+        for x, o in zip(patches, outs):
+            xd = x.double().numpy()
+            N, C = xd.shape[:2]
+            cg = C // G
+            y = np.empty_like(xd)
+            for i in range(N):
+                for ch in range(C):
+                    g = ch // cg
+                    z = (xd[i, ch] - mu[i, g]) / np.sqrt(var[i, g] + eps) * float(gamma[ch]) + float(beta[ch])
+                    y[i, ch] = z / (1.0 + np.exp(-z)) if silu else z
+            o.copy_(torch.from_numpy(y))
+        return outs
+
+
 def _stitch_share(tb, sharded, case, world, rank):
-    import numpy as np
-    from oracle.stitch import stitch as oracle_stitch
+    # this rank's tile rows through the module's own entry point
     at, ay, ax, B, C = STITCH_CASES[case]
     lt, ly, lx, B, C, tiles = _stitch_tiles(case)
-    lay = tb.tb_stitch_shard_layout(tb.Axis(*at) if at else None, tb.Axis(*ay), tb.Axis(*ax), B, C, world, rank)
+    a_t, a_y, a_x = (tb.Axis(*at) if at else None), tb.Axis(*ay), tb.Axis(*ax)
+    lay = tb.tb_stitch_shard_layout(a_t, a_y, a_x, B, C, world, rank)
     rb, re_ = lay.row_begin, lay.row_end
-    send = recv = None
-    if lay.send_elems:
-        # the raw last rows of every tile of the rank's last tile row
-        e = ly.blends[re_]
-        send = torch.cat([t[..., -e:, :].reshape(-1) for per_k in tiles for t in per_k[re_ - 1]])
-        assert send.numel() == lay.send_elems
-    if lay.halo_elems:
-        recv = torch.empty(lay.halo_elems, dtype=torch.int16)
-    sharded.exchange_halo(send, recv)
-    rows = []
-    for k, per_k in enumerate(tiles):
-        grid = []
-        if recv is not None:
-            band, off = [], sum(B * C * (lt.extents[kk] if lt else 1) * lay.halo_rows * sum(lx.extents)
-                                for kk in range(k))
-            for w in lx.extents:
-                shape = (B, C) + ((lt.extents[k],) if lt else ()) + (lay.halo_rows, w)
-                n = int(np.prod(shape))
-                band.append(recv[off:off + n].view(shape))
-                off += n
-            grid.append(band)
-        grid += per_k[rb:re_]
-        rows.append([[t.numpy().view(np.uint16) for t in row] for row in grid])
-    local_y = _local_axis(ly, rb, re_, lay.halo_rows)
-    out = None
-    if re_ > rb:
-        if lt:
-            out = oracle_stitch(rows, (lt, local_y, lx), "bf16")
-        else:
-            out = oracle_stitch(rows[0], (local_y, lx), "bf16")
-        out = out[..., local_y.kept[0] if lay.halo_rows else 0:, :]
-    return lay.out_row_begin, lay.out_rows, out
+    lib = _OracleLib(tb)
+    if at:
+        out = torch.empty((B, C, lt.out_extent, lay.out_rows, lx.out_extent), dtype=torch.int16)
+        sharded.stitch3d_row_sharded([per_k[rb:re_] for per_k in tiles], a_t, a_y, a_x, out, lib=lib)
+    else:
+        out = torch.empty((B, C, lay.out_rows, lx.out_extent), dtype=torch.int16)
+        sharded.stitch2d_row_sharded(tiles[0][rb:re_], a_y, a_x, out, lib=lib)
+    return lay.out_row_begin, lay.out_rows, (out.numpy().view("uint16") if lay.out_rows else None)
 
 
 def _stitch_rank(rank, world, port, q):
@@ -215,16 +278,17 @@ def _records(patch, G, parts):
 
 
 def _gn_rank(rank, world, port, q):
-    # Every rank holds one patch, writes its records (cut into a rank-dependent
-    # number of parts, as GPUs with other SM counts would), and one all-gather
-    # gives every rank the records of the whole tensor; pooling every record
-    # with elements gives the unsharded mean and biased variance.
+    # Every rank holds one patch; patch_group_norm_sharded writes its records
+    # (cut into a rank-dependent number of parts, as GPUs with other SM counts
+    # would), gathers every rank's records in one all-gather and normalises
+    # its own patch with the pooled statistics; the result must be the
+    # unsharded GroupNorm's patch.
     sys.path.insert(0, ROOT)
     import numpy as np
     from oracle import groupnorm as GN
     from patch_groupnorm_gb300 import build
     build.build()
-    from patch_groupnorm_gb300 import sharded
+    from patch_groupnorm_gb300 import sharded, tileblend as tb
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
@@ -233,22 +297,23 @@ def _gn_rank(rank, world, port, q):
         sizes = [4, 3, 3][:world]                     # ragged height bands
         starts = np.cumsum([0] + sizes[:-1])
         patches = [x[:, :, s:s + n] + (r - 1) * 2.0 for r, (s, n) in enumerate(zip(starts, sizes))]
-        every = sharded.gather_partials(_records(patches[rank], 4, 1 + 3 * rank), None).numpy()
-        assert every.shape == (world, 2, 4, 8, 2)
-        c = every[..., 0].astype(np.float64)
-        mv = np.ascontiguousarray(every[..., 1]).view(np.float32).reshape(every.shape[:-1] + (2,))
-        m, v = mv[..., 0].astype(np.float64), mv[..., 1].astype(np.float64)
-        c, m, v = (a.transpose(1, 2, 0, 3).reshape(2, 4, -1) for a in (c, m, v))
-        n = c.sum(-1)
-        mu = (c * m).sum(-1) / n
-        var = (v + c * (m - mu[..., None]) ** 2).sum(-1) / n
-        ref_mu, ref_var = GN.group_stats(patches, 4)
-        ok = np.abs(mu - ref_mu).max() < 1e-5 and np.abs(var / ref_var - 1).max() < 1e-5
-        q.put((rank, bool(ok)))
+        gamma = 1.0 + 0.1 * rng.standard_normal(12)
+        beta = 0.1 * rng.standard_normal(12)
+
+        class Lib(_OracleLib):
+            def tb_patch_gn_stats(self, ps, G, partials):
+                for p_, patch in enumerate(ps):
+                    partials[p_] = _records(patch.double().numpy(), G, 1 + 3 * rank)[0]
+
+        mine = torch.from_numpy(patches[rank].copy())
+        out = sharded.patch_group_norm_sharded([mine], 4, torch.from_numpy(gamma), torch.from_numpy(beta), 1e-6,
+                                               silu=True, lib=Lib(tb))[0]
+        want = GN.patch_group_norm(patches, 4, gamma, beta, 1e-6, silu=True)[rank]
+        q.put((rank, bool(np.abs(out.numpy() - want).max() < 1e-5)))
         dist.barrier()
     finally:
         dist.destroy_process_group()
 
 
-def test_groupnorm_records_all_gather_gives_the_pooled_statistics():
+def test_sharded_groupnorm_over_gloo_equals_the_unsharded_oracle():
     assert _spawn(_gn_rank, 3) == {r: True for r in range(3)}
