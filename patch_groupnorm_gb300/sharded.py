@@ -48,20 +48,23 @@ def _global(group, r: int) -> int:
 
 def exchange_halo(send: Optional[torch.Tensor], recv: Optional[torch.Tensor], group=None) -> None:
     """Send ``send`` to the next rank and receive ``recv`` from the previous
-    one (either may be None), as one batch of point-to-point transfers."""
+    one (either may be None).  Non-blocking point-to-point transfers posted
+    together and then waited on, so no rank waits for its successor before
+    receiving from its predecessor; a rank with nothing to exchange makes no
+    call (a batched exchange would need every rank of the group in it).  With
+    NCCL each rank's current CUDA device must be its own GPU."""
     world, rank = _world_rank(group)
-    ops = []
-    if send is not None:
-        if rank + 1 >= world:
-            raise ValueError("the last rank has no successor to send to")
-        ops.append(dist.P2POp(dist.isend, send, _global(group, rank + 1), group))
+    reqs = []
     if recv is not None:
         if rank == 0:
             raise ValueError("rank 0 has no predecessor to receive from")
-        ops.append(dist.P2POp(dist.irecv, recv, _global(group, rank - 1), group))
-    if ops:
-        for req in dist.batch_isend_irecv(ops):
-            req.wait()
+        reqs.append(dist.irecv(recv, _global(group, rank - 1), group=group))
+    if send is not None:
+        if rank + 1 >= world:
+            raise ValueError("the last rank has no successor to send to")
+        reqs.append(dist.isend(send, _global(group, rank + 1), group=group))
+    for req in reqs:
+        req.wait()
 
 
 def stitch2d_row_sharded(tiles: Sequence[Sequence[torch.Tensor]], ay: tb.Axis, ax: tb.Axis, out: torch.Tensor,
