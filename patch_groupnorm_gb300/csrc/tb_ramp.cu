@@ -309,9 +309,11 @@ __device__ __forceinline__ void run_rect(const RampParams& p, int sy, int sx, in
 // 16-byte path: weights precomputed per CTA, lane pairs in packed fp32
 // ---------------------------------------------------------------------------
 
-// Rows of a rectangle whose normalised height weights one CTA tabulates in
-// shared memory (longer multi-cover rectangles compute them per row).
-constexpr int RAMP_WY_CAP = 512;
+// Rows of a rectangle whose normalised height weights, and 16-byte columns
+// whose normalised width weights, one CTA tabulates in shared memory (larger
+// multi-cover rectangles compute them per row or per column).
+constexpr int RAMP_WY_CAP = 256;
+constexpr int RAMP_WX_CAP = 64;
 
 using u64 = unsigned long long;
 __device__ __forceinline__ u64 pk2(float lo, float hi) {
@@ -378,7 +380,8 @@ struct RowCursor {
 
 template <int CY, int CX, int DT>
 __device__ __forceinline__ void run_rect_vec(const RampParams& p, int sy, int sx, int fbeg, int fend,
-                                             uint32_t s_ring, const float* s_wy, bool wy_table) {
+                                             uint32_t s_ring, const float* s_wy, bool wy_table, const float* s_wx,
+                                             bool wx_table) {
     constexpr int VEC = 16 / RElt<DT>::BYTES;
     constexpr int NP = RElt<DT>::BYTES == 4 ? 2 : 4;  // lane pairs per chunk
     constexpr int NU = CY * CX;
@@ -430,17 +433,24 @@ __device__ __forceinline__ void run_rect_vec(const RampParams& p, int sy, int sx
         u64 wxp[CX][NP];
         if constexpr (CX > 1) {
             float wx[CX][VEC];
+            if (wx_table) {
 #pragma unroll
-            for (int l = 0; l < VEC; ++l) {
-                float sum = 0.f;
+                for (int l = 0; l < VEC; ++l)
 #pragma unroll
-                for (int b = 0; b < CX; ++b) {
-                    wx[b][l] = axis_w<CX>(AX, sx, b, x0 + l);
-                    sum += wx[b][l];
+                    for (int b = 0; b < CX; ++b) wx[b][l] = s_wx[(c * VEC + l) * CX + b];
+            } else {
+#pragma unroll
+                for (int l = 0; l < VEC; ++l) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int b = 0; b < CX; ++b) {
+                        wx[b][l] = axis_w<CX>(AX, sx, b, x0 + l);
+                        sum += wx[b][l];
+                    }
+                    const float inv = 1.0f / sum;
+#pragma unroll
+                    for (int b = 0; b < CX; ++b) wx[b][l] *= inv;
                 }
-                const float inv = 1.0f / sum;
-#pragma unroll
-                for (int b = 0; b < CX; ++b) wx[b][l] *= inv;
             }
 #pragma unroll
             for (int b = 0; b < CX; ++b)
@@ -544,6 +554,7 @@ template <int DT, int VEC>
 __global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_constant__ RampParams p) {
     extern __shared__ __align__(16) unsigned char s_ring[];
     __shared__ float s_wy[RAMP_WY_CAP * RAMP_MAXCOVER];
+    __shared__ float s_wx[RAMP_WX_CAP * 8 * RAMP_MAXCOVER];
     // A piece is a run of rows of one rectangle, in the rectangle's (plane,
     // row) space flattened over all planes.  blockIdx.y is the piece index and
     // blockIdx.x the rectangle, so the CTAs launched first cover every
@@ -576,7 +587,21 @@ __global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_consta
     // the rectangle's normalised height weights (parameters only)
     const int len = p.ay.seg_len[sy];
     const bool wy_table = cy > 1 && len <= RAMP_WY_CAP;
+    const int wcols = p.ax.seg_len[sx];  // samples
+    const bool wx_table = cx > 1 && wcols <= RAMP_WX_CAP * VEC;
     if constexpr (VEC * RElt<DT>::BYTES == 16) {
+        if (wx_table) {
+            const int x0 = p.ax.seg_start[sx];
+            for (int xl = threadIdx.x; xl < wcols; xl += RAMP_BLOCK) {
+                float w[RAMP_MAXCOVER], sum = 0.f;
+                for (int b = 0; b < cx; ++b) {
+                    w[b] = axis_w<1>(p.ax, sx, b, x0 + xl);
+                    sum += w[b];
+                }
+                const float inv = 1.0f / sum;
+                for (int b = 0; b < cx; ++b) s_wx[xl * cx + b] = w[b] * inv;
+            }
+        }
         if (wy_table) {
             const int y0 = p.ay.seg_start[sy];
             for (int yl = threadIdx.x; yl < len; yl += RAMP_BLOCK) {
@@ -588,13 +613,13 @@ __global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_consta
                 const float inv = 1.0f / sum;
                 for (int a = 0; a < cy; ++a) s_wy[yl * cy + a] = w[a] * inv;
             }
-            __syncthreads();
         }
+        if (wy_table || wx_table) __syncthreads();
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(s_ring);
     if constexpr (VEC * RElt<DT>::BYTES == 16) {
-#define TB_RECT(CY_, CX_) run_rect_vec<CY_, CX_, DT>(p, sy, sx, fbeg, fend, ring, s_wy, wy_table)
+#define TB_RECT(CY_, CX_) run_rect_vec<CY_, CX_, DT>(p, sy, sx, fbeg, fend, ring, s_wy, wy_table, s_wx, wx_table)
         switch (cy * 4 + cx) {
             case 5: TB_RECT(1, 1); break;
             case 6: TB_RECT(1, 2); break;
