@@ -282,6 +282,55 @@ tb_status tb_stitch3d_shard(const void* const* tiles, const void* halo, tb_dtype
                             void* stream);
 
 /*
+ * Frame-sharded video stitch: the same partition along the time axis of a 3D
+ * grid.  The frame tiles are dealt to the ranks; before stitching, rank r
+ * receives the raw last e_t(frame_begin) frames of every tile of rank
+ * r - 1's last frame tile.  The ranks' outputs, concatenated along the
+ * frames, equal tb_stitch3d bit for bit.
+ *
+ * tb_stitch_shard_frames_layout -- as tb_stitch_shard_layout, with the
+ * fields counting frame tiles and output frames (row_begin/row_end: frame
+ * tiles; out_row_begin/out_rows: output frames; halo_rows: e_t(frame_begin));
+ * `at` is required.
+ */
+tb_status tb_stitch_shard_frames_layout(const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int64_t B,
+                                        int64_t C, int32_t world, int32_t rank, tb_shard_layout* out);
+
+/*
+ * tb_stitch_halo_pack_frames -- the band a rank sends to its successor along
+ * the time axis: the last e_t(frame_tile + 1) frames of every tile of frame
+ * tile `frame_tile`, packed tile by tile in row-major (i, j) order, each
+ * [B, C, e_t(frame_tile + 1), L_y(i), L_x(j)].
+ *   tiles       host array of the n_y * n_x device pointers of the frame
+ *               tile, row-major (i, j)
+ *   frame_tile  0 .. n_t - 2
+ *   halo        device buffer of send_elems elements (see
+ *               tb_stitch_shard_frames_layout)
+ * Errors as tb_stitch_halo_pack.
+ */
+tb_status tb_stitch_halo_pack_frames(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
+                                     const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int32_t frame_tile,
+                                     void* halo, void* stream);
+
+/*
+ * tb_stitch3d_shard_frames -- frame tiles [frame_begin, frame_end) of a video
+ * grid stitched as tb_stitch3d would stitch them in the whole grid, into
+ * `out` ([B, C, out_frames, out_h, out_w]: the output frames
+ * [out_row_begin, out_row_begin + out_frames) of the full video).
+ *   tiles   host array of (frame_end - frame_begin) * n_y * n_x device
+ *           pointers, row-major over (k - frame_begin, i, j)
+ *   halo    the band tb_stitch_halo_pack_frames made of frame tile
+ *           frame_begin - 1; required when frame_begin > 0 and
+ *           e_t(frame_begin) > 0, else ignored
+ * Errors as tb_stitch3d, plus TB_ERR_SHAPE for a frame range outside
+ * [0, n_t] or out_frames that does not match it.
+ */
+tb_status tb_stitch3d_shard_frames(const void* const* tiles, const void* halo, tb_dtype dtype, int64_t B, int64_t C,
+                                   const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int32_t frame_begin,
+                                   int32_t frame_end, void* out, int64_t out_frames, int64_t out_h, int64_t out_w,
+                                   void* stream);
+
+/*
  * One axis of a normalised-ramp tile layout [STU]: n_tiles tiles of one
  * extent, placed by the caller (a planner spreads them so the first starts at
  * 0 and the last ends at out_extent).

@@ -526,9 +526,11 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     return TB_OK;
 }
 
-// Rows [row_begin, row_end) of the height axis, stitched by one rank of a
-// row-sharded stitch; `halo` holds the packed band of row row_begin - 1.
+// Tile rows (axis 1, height) or frame tiles (axis 0, time) [begin, end),
+// stitched by one rank of a sharded stitch; `halo` holds the packed band of
+// tile begin - 1 along that axis.
 struct Shard {
+    int axis;
     int32_t row_begin, row_end;
     const void* halo;
 };
@@ -591,31 +593,40 @@ tb_status stitch_common(int ndim, const void* const* tiles, tb_dtype dtype, int6
     bool halo = false;
     const void* table[TB_MAX_TILES];
     if (shard != nullptr) {
+        const int A = shard->axis;  // 0: frame tiles, 1: tile rows
         Axis l;
-        if (!shard_axis(g[1], shard->row_begin, shard->row_end, l, &halo)) return TB_ERR_SHAPE;
-        const int32_t rows_in = shard->row_end - shard->row_begin;
-        if ((int64_t)g[0].n * (rows_in + (halo ? 1 : 0)) * g[2].n > TB_MAX_TILES) return TB_ERR_UNSUPPORTED;
+        if (!shard_axis(g[A], shard->row_begin, shard->row_end, l, &halo)) return TB_ERR_SHAPE;
+        const int32_t in = shard->row_end - shard->row_begin;
+        const int h = halo ? 1 : 0;
+        const int nt = A == 0 ? in + h : g[0].n, ny = A == 1 ? in + h : g[1].n;
+        if ((int64_t)nt * ny * g[2].n > TB_MAX_TILES) return TB_ERR_UNSUPPORTED;
         if (halo && shard->halo == nullptr && B * C > 0) return TB_ERR_NULL;
-        if (tiles == nullptr && rows_in > 0 && B * C > 0) return TB_ERR_NULL;
+        if (tiles == nullptr && in > 0 && B * C > 0) return TB_ERR_NULL;
         const int eb = elem_bytes(dtype);
         const char* hp = reinterpret_cast<const char*>(shard->halo);
+        const int ny_in = A == 1 ? in : g[1].n;  // rows of the caller's own tiles
         int q = 0;
-        for (int k = 0; k < g[0].n; ++k) {
-            if (halo)
+        for (int k = 0; k < nt; ++k)
+            for (int i = 0; i < ny; ++i)
                 for (int j = 0; j < g[2].n; ++j) {
-                    table[q++] = hp;
-                    hp += B * C * (int64_t)g[0].ext[k] * l.ext[0] * g[2].ext[j] * eb;
+                    if (halo && ((A == 0 && k == 0) || (A == 1 && i == 0))) {
+                        // the halo tiles lie in the band in the order visited here
+                        table[q++] = hp;
+                        const int64_t lt = A == 0 ? l.ext[0] : g[0].ext[k];
+                        const int64_t ly = A == 1 ? l.ext[0] : g[1].ext[i];
+                        hp += B * C * lt * ly * g[2].ext[j] * eb;
+                    } else {
+                        const int kin = A == 0 ? k - h : k, iin = A == 1 ? i - h : i;
+                        table[q++] = tiles[((int64_t)kin * ny_in + iin) * g[2].n + j];
+                    }
                 }
-            for (int i = 0; i < rows_in; ++i)
-                for (int j = 0; j < g[2].n; ++j) table[q++] = tiles[((int64_t)k * rows_in + i) * g[2].n + j];
-        }
-        g[1] = l;
+        g[A] = l;
         tiles = table;
     }
     if ((ndim == 3 && out_t != g[0].out) || out_h != g[1].out || out_w != g[2].out) return TB_ERR_SHAPE;
     const int64_t planes = B * C;
     const int64_t ntiles = (int64_t)g[0].n * g[1].n * g[2].n;
-    if (planes == 0 || ntiles == 0 || g[1].out == 0) return TB_OK;  // nothing to write
+    if (planes == 0 || ntiles == 0 || g[0].out == 0 || g[1].out == 0) return TB_OK;  // nothing to write
     if (B > 0 && planes / B != C) return TB_ERR_SHAPE;
     if (tiles == nullptr || out == nullptr) return TB_ERR_NULL;
     if (ntiles > TB_MAX_TILES) return TB_ERR_UNSUPPORTED;
@@ -979,69 +990,76 @@ tb_status grid_axes(const tb_axis* at, const tb_axis* ay, const tb_axis* ax, Axi
     return derive_axis(ax, g[2], &ntot);
 }
 
-// Elements of the packed band of tile row `row`'s last e rows (all frame
-// tiles, all width tiles, all planes).
-int64_t band_elems(const Axis (&g)[3], int64_t planes, int32_t e) {
-    int64_t frames = 0, width = 0;
+// Elements of the packed band of `e` slices along `axis` (0: frames, 1: rows)
+// of every tile of one tile row (or frame tile), all planes.
+int64_t band_elems(const Axis (&g)[3], int axis, int64_t planes, int32_t e) {
+    int64_t frames = 0, rows = 0, width = 0;
     for (int k = 0; k < g[0].n; ++k) frames += g[0].ext[k];
+    for (int i = 0; i < g[1].n; ++i) rows += g[1].ext[i];
     for (int j = 0; j < g[2].n; ++j) width += g[2].ext[j];
-    return planes * frames * (int64_t)e * width;
+    return axis == 0 ? planes * (int64_t)e * rows * width : planes * frames * (int64_t)e * width;
 }
 
-TB_API tb_status tb_stitch_shard_layout(const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int64_t B, int64_t C,
-                                        int32_t world, int32_t rank, tb_shard_layout* out) {
-    if (ay == nullptr || ax == nullptr || out == nullptr) return TB_ERR_NULL;
+tb_status shard_layout(int axis, const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int64_t B, int64_t C,
+                       int32_t world, int32_t rank, tb_shard_layout* out) {
+    if (ay == nullptr || ax == nullptr || out == nullptr || (axis == 0 && at == nullptr)) return TB_ERR_NULL;
     if (B < 0 || C < 0 || world < 1 || rank < 0 || rank >= world) return TB_ERR_SHAPE;
     if (B > 0 && C > INT64_MAX / B) return TB_ERR_SHAPE;
     Axis g[3];
     tb_status s = grid_axes(at, ay, ax, g);
     if (s != TB_OK) return s;
-    // tile rows shared out in rank order, the first ranks one row more
-    const int32_t n = g[1].n, each = n / world, extra = n % world;
+    const Axis& a = g[axis];
+    // tiles along the axis shared out in rank order, the first ranks one more
+    const int32_t n = a.n, each = n / world, extra = n % world;
     const int32_t begin = rank * each + std::min(rank, extra);
     const int32_t end = begin + each + (rank < extra ? 1 : 0);
     tb_shard_layout l{};
     l.row_begin = begin;
     l.row_end = end;
-    for (int i = 0; i < begin; ++i) l.out_row_begin += g[1].kept[i];
-    for (int i = begin; i < end; ++i) l.out_rows += g[1].kept[i];
+    for (int i = 0; i < begin; ++i) l.out_row_begin += a.kept[i];
+    for (int i = begin; i < end; ++i) l.out_rows += a.kept[i];
     const int64_t planes = B * C;
-    if (end > begin && begin > 0 && g[1].blend[begin] > 0) {
-        l.halo_rows = g[1].blend[begin];
-        l.halo_elems = band_elems(g, planes, l.halo_rows);
+    if (end > begin && begin > 0 && a.blend[begin] > 0) {
+        l.halo_rows = a.blend[begin];
+        l.halo_elems = band_elems(g, axis, planes, l.halo_rows);
     }
-    if (end > begin && end < n && g[1].blend[end] > 0) l.send_elems = band_elems(g, planes, g[1].blend[end]);
+    if (end > begin && end < n && a.blend[end] > 0) l.send_elems = band_elems(g, axis, planes, a.blend[end]);
     *out = l;
     return TB_OK;
 }
 
-TB_API tb_status tb_stitch_halo_pack(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
-                                     const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int32_t row, void* halo,
-                                     void* stream) {
+// Packs the last e(index + 1) slices along `axis` of every tile of tile row
+// (axis 1) or frame tile (axis 0) `index`: tiles are the n_t x n_x tiles of
+// the row (k-major) or the n_y x n_x tiles of the frame tile (i-major).
+tb_status halo_pack(int axis, const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C, const tb_axis* at,
+                    const tb_axis* ay, const tb_axis* ax, int32_t index, void* halo, void* stream) {
     if (dtype != TB_F32 && dtype != TB_F16 && dtype != TB_BF16) return TB_ERR_DTYPE;
-    if (ay == nullptr || ax == nullptr) return TB_ERR_NULL;
+    if (ay == nullptr || ax == nullptr || (axis == 0 && at == nullptr)) return TB_ERR_NULL;
     if (B < 0 || C < 0) return TB_ERR_SHAPE;
     if (B > 0 && C > INT64_MAX / B) return TB_ERR_SHAPE;
     Axis g[3];
     tb_status s = grid_axes(at, ay, ax, g);
     if (s != TB_OK) return s;
-    if (row < 0 || row + 1 >= g[1].n) return TB_ERR_SHAPE;
-    const int32_t e = g[1].blend[row + 1];
+    if (index < 0 || index + 1 >= g[axis].n) return TB_ERR_SHAPE;
+    const int32_t e = g[axis].blend[index + 1];
     const int64_t planes = B * C;
     if (e == 0 || planes == 0) return TB_OK;
-    const int64_t ntiles = (int64_t)g[0].n * g[2].n;
+    const int nouter = axis == 0 ? g[1].n : g[0].n;  // tiles of the row / frame tile: nouter x n_x
+    const int64_t ntiles = (int64_t)nouter * g[2].n;
     if (ntiles > tb::HALO_MAXT) return TB_ERR_UNSUPPORTED;
     if (tiles == nullptr || halo == nullptr) return TB_ERR_NULL;
     for (int64_t q = 0; q < ntiles; ++q)
         if (tiles[q] == nullptr) return TB_ERR_NULL;
     const int eb = elem_bytes(dtype);
-    // widest chunk dividing every row, band offset and address
+    // widest chunk dividing every slice, band offset and address
     int vb = 16;
     auto fit = [&vb](uint64_t v) {
         while (vb > 1 && v % (uint64_t)vb != 0) vb >>= 1;
     };
     fit((uint64_t)reinterpret_cast<uintptr_t>(halo));
-    for (int j = 0; j < g[2].n; ++j) fit((uint64_t)g[2].ext[j] * eb);
+    for (int o = 0; o < nouter; ++o)
+        for (int j = 0; j < g[2].n; ++j)
+            fit((uint64_t)(axis == 0 ? (int64_t)g[1].ext[o] * g[2].ext[j] : (int64_t)g[2].ext[j]) * eb);
     for (int64_t q = 0; q < ntiles; ++q) fit((uint64_t)reinterpret_cast<uintptr_t>(tiles[q]));
     tb::HaloPackParams prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -1049,17 +1067,21 @@ TB_API tb_status tb_stitch_halo_pack(const void* const* tiles, tb_dtype dtype, i
     prm.status = debug_status();
     prm.e = e;
     prm.ntiles = (int32_t)ntiles;
-    const int64_t ly = g[1].ext[row];
+    // a tile is [planes][outer slices][slices along the axis][slice], so a
+    // band is the last e slices of each (plane, outer slice)
     int64_t off = 0, most = 0;
-    for (int k = 0; k < g[0].n; ++k)
+    for (int o = 0; o < nouter; ++o)
         for (int j = 0; j < g[2].n; ++j) {
-            const int64_t q = (int64_t)k * g[2].n + j;
-            const int64_t w = (int64_t)g[2].ext[j] * eb / vb;
-            if (w > 2147483647LL || planes * g[0].ext[k] * ly * w > (INT64_MAX >> 1)) return TB_ERR_UNSUPPORTED;
+            const int64_t q = (int64_t)o * g[2].n + j;
+            const int64_t slices = axis == 0 ? g[0].ext[index] : g[1].ext[index];
+            const int64_t outer = axis == 0 ? 1 : g[0].ext[o];
+            const int64_t w = (axis == 0 ? (int64_t)g[1].ext[o] * g[2].ext[j] : (int64_t)g[2].ext[j]) * eb / vb;
+            if (w > 2147483647LL || slices > 2147483647LL || planes * outer * slices * w > (INT64_MAX >> 1))
+                return TB_ERR_UNSUPPORTED;
             prm.src[q] = tiles[q];
-            prm.rows[q] = (int32_t)ly;
+            prm.rows[q] = (int32_t)slices;
             prm.width[q] = (int32_t)w;
-            prm.n[q] = planes * g[0].ext[k] * e * w;
+            prm.n[q] = planes * outer * e * w;
             prm.dst_off[q] = off;
             off += prm.n[q];
             most = std::max(most, prm.n[q]);
@@ -1075,10 +1097,32 @@ TB_API tb_status tb_stitch_halo_pack(const void* const* tiles, tb_dtype dtype, i
     return TB_OK;
 }
 
+TB_API tb_status tb_stitch_shard_layout(const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int64_t B, int64_t C,
+                                        int32_t world, int32_t rank, tb_shard_layout* out) {
+    return shard_layout(1, at, ay, ax, B, C, world, rank, out);
+}
+
+TB_API tb_status tb_stitch_shard_frames_layout(const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int64_t B,
+                                               int64_t C, int32_t world, int32_t rank, tb_shard_layout* out) {
+    return shard_layout(0, at, ay, ax, B, C, world, rank, out);
+}
+
+TB_API tb_status tb_stitch_halo_pack(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
+                                     const tb_axis* at, const tb_axis* ay, const tb_axis* ax, int32_t row, void* halo,
+                                     void* stream) {
+    return halo_pack(1, tiles, dtype, B, C, at, ay, ax, row, halo, stream);
+}
+
+TB_API tb_status tb_stitch_halo_pack_frames(const void* const* tiles, tb_dtype dtype, int64_t B, int64_t C,
+                                            const tb_axis* at, const tb_axis* ay, const tb_axis* ax,
+                                            int32_t frame_tile, void* halo, void* stream) {
+    return halo_pack(0, tiles, dtype, B, C, at, ay, ax, frame_tile, halo, stream);
+}
+
 TB_API tb_status tb_stitch2d_shard(const void* const* tiles, const void* halo, tb_dtype dtype, int64_t B, int64_t C,
                                    const tb_axis* ay, const tb_axis* ax, int32_t row_begin, int32_t row_end,
                                    void* out, int64_t out_rows, int64_t out_w, void* stream) {
-    const Shard sh{row_begin, row_end, halo};
+    const Shard sh{1, row_begin, row_end, halo};
     return stitch_common(2, tiles, dtype, B, C, nullptr, ay, ax, out, 1, out_rows, out_w, stream, &sh);
 }
 
@@ -1087,8 +1131,17 @@ TB_API tb_status tb_stitch3d_shard(const void* const* tiles, const void* halo, t
                                    int32_t row_end, void* out, int64_t out_t, int64_t out_rows, int64_t out_w,
                                    void* stream) {
     if (at == nullptr) return TB_ERR_NULL;
-    const Shard sh{row_begin, row_end, halo};
+    const Shard sh{1, row_begin, row_end, halo};
     return stitch_common(3, tiles, dtype, B, C, at, ay, ax, out, out_t, out_rows, out_w, stream, &sh);
+}
+
+TB_API tb_status tb_stitch3d_shard_frames(const void* const* tiles, const void* halo, tb_dtype dtype, int64_t B,
+                                          int64_t C, const tb_axis* at, const tb_axis* ay, const tb_axis* ax,
+                                          int32_t frame_begin, int32_t frame_end, void* out, int64_t out_frames,
+                                          int64_t out_h, int64_t out_w, void* stream) {
+    if (at == nullptr) return TB_ERR_NULL;
+    const Shard sh{0, frame_begin, frame_end, halo};
+    return stitch_common(3, tiles, dtype, B, C, at, ay, ax, out, out_frames, out_h, out_w, stream, &sh);
 }
 
 TB_API tb_status tb_ramp_axis_spread(int32_t latent_extent, int32_t latent_tile, int32_t n_tiles, int32_t scale,

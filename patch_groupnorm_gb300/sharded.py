@@ -109,6 +109,26 @@ def stitch3d_row_sharded(tiles, at: tb.Axis, ay: tb.Axis, ax: tb.Axis, out: torc
     return lib.tb_stitch3d_shard(tiles, recv, at, ay, ax, lay.row_begin, lay.row_end, out)
 
 
+def stitch3d_frame_sharded(tiles, at: tb.Axis, ay: tb.Axis, ax: tb.Axis, out: torch.Tensor, group=None,
+                           lib=tb) -> torch.Tensor:
+    """This rank's frames of a video stitch sharded along the time axis:
+    ``tiles[k][i][j]`` over the rank's frame tiles k and all tile rows and
+    columns; ``out`` is [B, C, out_frames, H, W]."""
+    world, rank = _world_rank(group)
+    B, C = out.shape[:2]
+    lay = lib.tb_stitch_shard_frames_layout(at, ay, ax, B, C, world, rank)
+    if len(tiles) != lay.row_end - lay.row_begin:
+        raise ValueError("rank %d holds frame tiles [%d, %d)" % (rank, lay.row_begin, lay.row_end))
+    send = recv = None
+    if lay.send_elems:
+        send = torch.empty(lay.send_elems, dtype=out.dtype, device=out.device)
+        lib.tb_stitch_halo_pack_frames(tiles[-1], at, ay, ax, lay.row_end - 1, send)
+    if lay.halo_elems:
+        recv = torch.empty(lay.halo_elems, dtype=out.dtype, device=out.device)
+    exchange_halo(send, recv, group)
+    return lib.tb_stitch3d_shard_frames(tiles, recv, at, ay, ax, lay.row_begin, lay.row_end, out)
+
+
 def gather_partials(local: torch.Tensor, group=None) -> torch.Tensor:
     """Every rank's GroupNorm records, rank after rank: one all-gather of the
     [P, N, G, TB_GN_PARTS, 2] record buffers (all ranks hold P patches)."""

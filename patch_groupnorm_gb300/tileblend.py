@@ -98,6 +98,15 @@ _lib.tb_stitch_halo_pack.argtypes = [_P_vp, ctypes.c_int, _i64, _i64, _P_axis, _
 _lib.tb_stitch2d_shard.restype = ctypes.c_int
 _lib.tb_stitch2d_shard.argtypes = [_P_vp, _vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _i32, _i32, _vp, _i64,
                                    _i64, _vp]
+_lib.tb_stitch_shard_frames_layout.restype = ctypes.c_int
+_lib.tb_stitch_shard_frames_layout.argtypes = [_P_axis, _P_axis, _P_axis, _i64, _i64, _i32, _i32,
+                                               ctypes.POINTER(tb_shard_layout)]
+_lib.tb_stitch_halo_pack_frames.restype = ctypes.c_int
+_lib.tb_stitch_halo_pack_frames.argtypes = [_P_vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _P_axis, _i32, _vp,
+                                            _vp]
+_lib.tb_stitch3d_shard_frames.restype = ctypes.c_int
+_lib.tb_stitch3d_shard_frames.argtypes = [_P_vp, _vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _P_axis, _i32,
+                                          _i32, _vp, _i64, _i64, _i64, _vp]
 _lib.tb_stitch3d_shard.restype = ctypes.c_int
 _lib.tb_stitch3d_shard.argtypes = [_P_vp, _vp, ctypes.c_int, _i64, _i64, _P_axis, _P_axis, _P_axis, _i32, _i32, _vp,
                                    _i64, _i64, _i64, _vp]
@@ -127,7 +136,8 @@ EXPORTED = ("tb_version", "tb_status_string", "tb_last_cuda_error", "tb_axis_lay
             "tb_stitch3d", "tb_stitch_shard_layout", "tb_stitch_halo_pack", "tb_stitch2d_shard",
             "tb_stitch3d_shard", "tb_stitch2d_ramp", "tb_patch_gn_stats", "tb_patch_gn_apply",
             "tb_patch_gn_apply_gathered", "tb_patch_group_norm_noalloc", "tb_patchify_layout", "tb_patchify",
-            "tb_gather_patches", "tb_device_status", "tb_ramp_axis_spread")
+            "tb_gather_patches", "tb_device_status", "tb_ramp_axis_spread", "tb_stitch_shard_frames_layout",
+            "tb_stitch_halo_pack_frames", "tb_stitch3d_shard_frames")
 
 
 class TileBlendError(RuntimeError):
@@ -396,6 +406,59 @@ def tb_stitch3d_shard(tiles, halo: Optional[torch.Tensor], at: Axis, ay: Axis, a
     _check(_lib.tb_stitch3d_shard(_ptr_array([t.data_ptr() for t in flat]), hp, _dtype_code(out), B, C,
                                   ctypes.byref(a_t), ctypes.byref(a_y), ctypes.byref(a_x), row_begin, row_end,
                                   out.data_ptr(), T, H, W, _stream_handle(stream)), "tb_stitch3d_shard")
+    return out
+
+
+def tb_stitch_shard_frames_layout(at: Axis, ay: Axis, ax: Axis, B: int, C: int, world: int,
+                                  rank: int) -> ShardLayout:
+    """Rank ``rank``'s share of a video stitch whose frame tiles are split
+    over ``world`` ranks (host only; the fields count frame tiles and output
+    frames)."""
+    a_t, a_y, a_x = at.c(), ay.c(), ax.c()
+    out = tb_shard_layout()
+    _check(_lib.tb_stitch_shard_frames_layout(ctypes.byref(a_t), ctypes.byref(a_y), ctypes.byref(a_x), B, C, world,
+                                              rank, ctypes.byref(out)), "tb_stitch_shard_frames_layout")
+    return ShardLayout(out.row_begin, out.row_end, out.out_row_begin, out.out_rows, out.halo_rows, out.halo_elems,
+                       out.send_elems)
+
+
+def tb_stitch_halo_pack_frames(frame_tiles, at: Axis, ay: Axis, ax: Axis, frame_tile: int, halo: torch.Tensor,
+                               stream=None) -> torch.Tensor:
+    """Pack the last e_t(frame_tile + 1) frames of every tile of frame tile
+    ``frame_tile`` (``frame_tiles[i][j]``) into ``halo``."""
+    flat = [t for row in frame_tiles for t in row]
+    for q, t in enumerate(flat):
+        _cuda_contig(t, "tile %d" % q)
+    _cuda_contig(halo, "halo")
+    B, C = flat[0].shape[:2]
+    a_t, a_y, a_x = at.c(), ay.c(), ax.c()
+    _check(_lib.tb_stitch_halo_pack_frames(_ptr_array([t.data_ptr() for t in flat]), _dtype_code(halo), B, C,
+                                           ctypes.byref(a_t), ctypes.byref(a_y), ctypes.byref(a_x), frame_tile,
+                                           halo.data_ptr(), _stream_handle(stream)), "tb_stitch_halo_pack_frames")
+    return halo
+
+
+def tb_stitch3d_shard_frames(tiles, halo: Optional[torch.Tensor], at: Axis, ay: Axis, ax: Axis, frame_begin: int,
+                             frame_end: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Stitch frame tiles [frame_begin, frame_end) (``tiles[k - frame_begin][i][j]``)
+    with the band ``halo`` of the frame tile before into ``out``
+    ([B, C, out_frames, H, W])."""
+    _cuda_contig(out, "out")
+    B, C, T, H, W = out.shape
+    flat = _flat_tiles(tiles, 3)
+    for q, t in enumerate(flat):
+        _cuda_contig(t, "tile %d" % q)
+        if t.dtype != out.dtype:
+            raise ValueError("tile %d has dtype %s, out %s" % (q, t.dtype, out.dtype))
+    hp = None
+    if halo is not None:
+        _cuda_contig(halo, "halo")
+        hp = halo.data_ptr()
+    a_t, a_y, a_x = at.c(), ay.c(), ax.c()
+    _check(_lib.tb_stitch3d_shard_frames(_ptr_array([t.data_ptr() for t in flat]), hp, _dtype_code(out), B, C,
+                                         ctypes.byref(a_t), ctypes.byref(a_y), ctypes.byref(a_x), frame_begin,
+                                         frame_end, out.data_ptr(), T, H, W, _stream_handle(stream)),
+           "tb_stitch3d_shard_frames")
     return out
 
 

@@ -290,3 +290,72 @@ def test_sharded_module_on_a_one_rank_nccl_group(tbl):
             assert torch.equal(o.view(torch.int16), r.view(torch.int16))
     finally:
         dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# frame-sharded video stitch
+# --------------------------------------------------------------------------
+
+def _frame_sharded_gpu(tbl, tiles_cpu, axes, dtype, B, C, world):
+    """Every rank's frame tiles, run in rank order on one GPU; returns the
+    ranks' outputs concatenated along the frames."""
+    at, ay, ax = [_axis(tbl, a) for a in axes]
+    lays = [axis_layout(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in axes]
+    dev = [[[t.cuda() for t in row] for row in pl] for pl in tiles_cpu]
+    outs, bands = [], {}
+    for r in range(world):
+        lay = tbl.tb_stitch_shard_frames_layout(at, ay, ax, B, C, world, r)
+        mine = dev[lay.row_begin:lay.row_end]
+        out = torch.full((B, C, lay.out_rows, lays[1].out_extent, lays[2].out_extent), float("nan"),
+                         dtype=TORCH[dtype], device="cuda")
+        halo = bands.get(r)
+        assert (halo is None) == (lay.halo_elems == 0)
+        tbl.tb_stitch3d_shard_frames(mine, halo, at, ay, ax, lay.row_begin, lay.row_end, out)
+        if lay.send_elems:
+            send = torch.empty(lay.send_elems, dtype=TORCH[dtype], device="cuda")
+            tbl.tb_stitch_halo_pack_frames(mine[-1], at, ay, ax, lay.row_end - 1, send)
+            bands[r + 1] = send
+        outs.append(out)
+    torch.cuda.synchronize()
+    return torch.cat([o.cpu() for o in outs], dim=2)
+
+
+def test_full_video_frame_sharded_bit_exact(tbl):
+    w = W.STITCH["video_49x480x832_bf16"]
+    lays = [axis_layout(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in w.axes]
+    tiles = W.make_stitch_tiles(w, [boxes(l, a.scale) for l, a in zip(lays, w.axes)], [l.out_extent for l in lays])
+    ref = oracle_stitch(_storage_grid(tiles, w.dtype), lays, w.dtype)
+    for world in (2, 3, lays[0].n, lays[0].n + 2):
+        _check_equal(_frame_sharded_gpu(tbl, tiles, w.axes, w.dtype, w.B, w.C, world), ref, w.dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_random_small_videos_frame_sharded_bit_exact(tbl, dtype):
+    rnd = random.Random(77 + len(dtype))
+    rng = np.random.default_rng(78)
+    for trial in range(8):
+        axes = _random_axes(rnd, 3)
+        lays = [axis_layout(a.latent_extent, a.latent_tile, a.overlap, a.scale) for a in axes]
+        B, C = rnd.randint(1, 2), rnd.randint(1, 3)
+        tiles = [[[torch.from_numpy(rng.uniform(-1, 1, (B, C, lt, ly, lx))).to(TORCH[dtype])
+                   for lx in lays[2].extents] for ly in lays[1].extents] for lt in lays[0].extents]
+        ref = oracle_stitch(_storage_grid(tiles, dtype), lays, dtype)
+        for world in (2, 3):
+            _check_equal(_frame_sharded_gpu(tbl, tiles, axes, dtype, B, C, world), ref, dtype)
+
+
+def test_frame_halo_pack_is_the_last_frames_of_each_tile(tbl):
+    w = W.STITCH["video_49x480x832_bf16"]
+    at, ay, ax = [_axis(tbl, a) for a in w.axes]
+    lays = [tbl.tb_axis_layout(a) for a in (at, ay, ax)]
+    rng = np.random.default_rng(12)
+    k = 1
+    e = lays[0].blends[k + 1]
+    tiles = [[torch.from_numpy(rng.uniform(-1, 1, (1, 3, lays[0].extents[k], ly, lx))).to(torch.bfloat16).cuda()
+              for lx in lays[2].extents] for ly in lays[1].extents]
+    lay = tbl.tb_stitch_shard_frames_layout(at, ay, ax, 1, 3, 5, k)
+    send = torch.empty(lay.send_elems, dtype=torch.bfloat16, device="cuda")
+    tbl.tb_stitch_halo_pack_frames(tiles, at, ay, ax, k, send)
+    want = torch.cat([t[:, :, -e:].reshape(-1) for row in tiles for t in row])
+    torch.cuda.synchronize()
+    assert torch.equal(send.view(torch.int16), want.view(torch.int16))

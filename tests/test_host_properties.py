@@ -74,3 +74,20 @@ def test_ramp_spread_accepts_exactly_the_covering_layouts(tbl, ext, tile, n, sca
     assert list(org[:n]) == evenly_spread_origins(ext, tile, n, scale)
     assert (a.n_tiles, a.tile_extent, a.out_extent, a.zero, a.ramp) == (n, tile * scale, ext * scale, zero * scale,
                                                                         ramp * scale)
+
+
+@settings(max_examples=200, deadline=None)
+@given(at=axis_args, ay=axis_args, ax=axis_args, B=st.integers(0, 3), C=st.integers(0, 3), world=st.integers(1, 9))
+def test_frame_shard_layout_partitions_the_frames_and_the_bands_match(tbl, at, ay, ax, B, C, world):
+    lt, ly, lx = _ok_axis(at), _ok_axis(ay), _ok_axis(ax)
+    if lt is None or ly is None or lx is None:
+        return
+    shares = [tbl.tb_stitch_shard_frames_layout(tbl.Axis(*at), tbl.Axis(*ay), tbl.Axis(*ax), B, C, world, r)
+              for r in range(world)]
+    assert shares[0].row_begin == 0 and shares[-1].row_end == lt.n
+    assert sum(s.out_rows for s in shares) == lt.out_extent
+    for a, b in zip(shares, shares[1:]):
+        assert a.row_end == b.row_begin
+        if b.row_end > b.row_begin:
+            assert a.send_elems == b.halo_elems
+            assert b.halo_elems == B * C * b.halo_rows * sum(ly.extents) * sum(lx.extents)

@@ -325,6 +325,22 @@ def test_shard_layout_matches_the_oracle_geometry(tbl, case):
         assert sum(w[3] for w in want) == ly.out_extent
 
 
+@pytest.mark.parametrize("case", [
+    ((49, 16, 0.25, 1), (60, 32, 0.25, 8), (104, 32, 0.25, 8), 1, 3),
+    ((21, 8, 0.25, 1), (40, 16, 0.25, 4), (24, 16, 0.25, 4), 2, 2),
+])
+def test_frame_shard_layout_matches_the_oracle_geometry(tbl, case):
+    at, ay, ax, B, C = case
+    lt, ly, lx = axis_layout(*at), axis_layout(*ay), axis_layout(*ax)
+    for world in (1, 2, 3, lt.n, lt.n + 3):
+        # frame tiles dealt like rows; a band is e_t frames of every (i, j) tile
+        want = _expected_shares(lt, world, B * C, 1, sum(ly.extents) * sum(lx.extents))
+        for r in range(world):
+            got = tbl.tb_stitch_shard_frames_layout(tbl.Axis(*at), tbl.Axis(*ay), tbl.Axis(*ax), B, C, world, r)
+            assert (got.row_begin, got.row_end, got.out_row_begin, got.out_rows, got.halo_rows, got.halo_elems,
+                    got.send_elems) == want[r], (world, r)
+
+
 def test_shard_calls_reject_before_launch(tbl):
     ay, ax = tbl.Axis(256, 64, 0.25, 8), tbl.Axis(128, 64, 0.25, 8)
     a_y, a_x = ay.c(), ax.c()
@@ -353,6 +369,17 @@ def test_shard_calls_reject_before_launch(tbl):
         == tbl.TB_ERR_SHAPE
     # an empty share writes nothing
     assert st(None, None, 2, 1, 3, ctypes.byref(a_y), ctypes.byref(a_x), 6, 6, None, 0, 1024, None) == tbl.TB_OK
+    # the frame forms need the frame axis
+    f = tbl._lib.tb_stitch_shard_frames_layout
+    assert f(None, ctypes.byref(a_y), ctypes.byref(a_x), 1, 3, 2, 0, ctypes.byref(out)) == tbl.TB_ERR_NULL
+    pf = tbl._lib.tb_stitch_halo_pack_frames
+    assert pf(arr, 2, 1, 3, None, ctypes.byref(a_y), ctypes.byref(a_x), 0, 16, None) == tbl.TB_ERR_NULL
+    a_t = tbl.Axis(49, 16, 0.25, 1).c()
+    assert pf(arr, 2, 1, 3, ctypes.byref(a_t), ctypes.byref(a_y), ctypes.byref(a_x), 4, 16, None) == tbl.TB_ERR_SHAPE
+    sf = tbl._lib.tb_stitch3d_shard_frames
+    # frame tiles 2..5 need the band of frame tile 1
+    assert sf(tiles, None, 2, 1, 3, ctypes.byref(a_t), ctypes.byref(a_y), ctypes.byref(a_x), 2, 5, 16, 25, 1536,
+              1024, None) == tbl.TB_ERR_NULL
 
 
 def test_gathered_apply_rejects_before_launch(tbl):

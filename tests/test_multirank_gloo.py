@@ -1,8 +1,9 @@
 """Multi-rank paths on CPU ranks over gloo: the benchmark's (one process per
 rank at world size 2, the slowest rank's time taken as the job's, the
-reference arm on rank 0 only), the row-sharded stitch (the library's rank
-layout and the halo exchange of patch_groupnorm_gb300.sharded at world sizes
-2 and 3, the CPU oracle standing in for the stitch kernel on every rank),
+reference arm on rank 0 only), the row- and frame-sharded stitch (the
+library's rank layout and patch_groupnorm_gb300.sharded's own entry points
+at world sizes 2 and 3, the CPU oracle standing in for the kernels on every
+rank),
 and the sharded PatchGroupNorm (every rank's records in the library's layout,
 one all-gather, pooled to the unsharded statistics)."""
 import os
@@ -174,6 +175,39 @@ class _OracleLib:
     def tb_stitch3d_shard(self, tiles, halo, at, ay, ax, rb, re_, out):
         return self._shard(tiles, halo, at, ay, ax, rb, re_, out)
 
+    def tb_stitch_shard_frames_layout(self, *args):
+        return self.tb.tb_stitch_shard_frames_layout(*args)
+
+    def tb_stitch_halo_pack_frames(self, frame_tiles, at, ay, ax, k, halo):
+        e = self._lay(at).blends[k + 1]
+        halo.copy_(torch.cat([t[:, :, -e:].reshape(-1) for row in frame_tiles for t in row]))
+
+    def tb_stitch3d_shard_frames(self, tiles, halo, at, ay, ax, fb, fe, out):
+        import numpy as np
+        from oracle.stitch import stitch as oracle_stitch
+        lt, ly, lx = self._lay(at), self._lay(ay), self._lay(ax)
+        B, C = out.shape[:2]
+        e = lt.blends[fb] if fb > 0 else 0
+        grid3 = []
+        if halo is not None and e:
+            off, plane = 0, []
+            for h in ly.extents:
+                row = []
+                for w in lx.extents:
+                    shape = (B, C, e, h, w)
+                    n = int(np.prod(shape))
+                    row.append(halo[off:off + n].view(shape))
+                    off += n
+                plane.append(row)
+            grid3.append(plane)
+        grid3 += list(tiles)
+        raw = [[[t.numpy().view(np.uint16) for t in r] for r in pl] for pl in grid3]
+        local_t = _local_axis(lt, fb, fe, e if halo is not None else 0)
+        res = oracle_stitch(raw, (local_t, ly, lx), "bf16")
+        res = res[:, :, local_t.kept[0] if (halo is not None and e) else 0:]
+        out.copy_(torch.from_numpy(np.ascontiguousarray(res).view(np.int16)))
+        return out
+
     def new_partials(self, P, N, G, device=None):
         return torch.zeros((P, N, G, 8, 2), dtype=torch.int64)
 
@@ -222,6 +256,17 @@ def _stitch_share(tb, sharded, case, world, rank):
     return lay.out_row_begin, lay.out_rows, (out.numpy().view("uint16") if lay.out_rows else None)
 
 
+def _frame_share(tb, sharded, world, rank):
+    # the video case sharded along the time axis, through the module
+    at, ay, ax, B, C = STITCH_CASES["video"]
+    lt, ly, lx, B, C, tiles = _stitch_tiles("video")
+    a_t, a_y, a_x = tb.Axis(*at), tb.Axis(*ay), tb.Axis(*ax)
+    lay = tb.tb_stitch_shard_frames_layout(a_t, a_y, a_x, B, C, world, rank)
+    out = torch.empty((B, C, lay.out_rows, ly.out_extent, lx.out_extent), dtype=torch.int16)
+    sharded.stitch3d_frame_sharded(tiles[lay.row_begin:lay.row_end], a_t, a_y, a_x, out, lib=_OracleLib(tb))
+    return lay.out_row_begin, lay.out_rows, (out.numpy().view("uint16") if lay.out_rows else None)
+
+
 def _stitch_rank(rank, world, port, q):
     sys.path.insert(0, ROOT)
     from patch_groupnorm_gb300 import build
@@ -230,7 +275,9 @@ def _stitch_rank(rank, world, port, q):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        q.put((rank, {case: _stitch_share(tb, sharded, case, world, rank) for case in STITCH_CASES}))
+        got = {case: _stitch_share(tb, sharded, case, world, rank) for case in STITCH_CASES}
+        got["video_frames"] = _frame_share(tb, sharded, world, rank)
+        q.put((rank, got))
         dist.barrier()
     finally:
         dist.destroy_process_group()
@@ -250,6 +297,13 @@ def test_row_sharded_stitch_over_gloo_equals_the_unsharded_oracle(world):
         assert [p[0] for p in parts] == [sum(p[1] for p in parts[:r]) for r in range(world)], case
         whole = np.concatenate([p[2] for p in parts if p[1] > 0], axis=-2)
         assert np.array_equal(whole, ref), case
+    # the video, sharded along the frames instead
+    lt, ly, lx, B, C, tiles = _stitch_tiles("video")
+    raw = [[[t.numpy().view(np.uint16) for t in row] for row in per_k] for per_k in tiles]
+    ref = oracle_stitch(raw, (lt, ly, lx), "bf16")
+    parts = [got[r]["video_frames"] for r in range(world)]
+    assert sum(p[1] for p in parts) == lt.out_extent
+    assert np.array_equal(np.concatenate([p[2] for p in parts if p[1] > 0], axis=2), ref)
 
 
 # --------------------------------------------------------------------------
