@@ -1259,7 +1259,9 @@ TB_API tb_status tb_stitch2d_ramp(const void* const* tiles, tb_dtype dtype, int6
         if (total >= (int64_t)TB_RAMP_PIECES_PER_SM * sms || rpt <= 2) break;
     }
     if (max_pieces > 65535) return TB_ERR_UNSUPPORTED;
-    cudaError_t e = tb::launch_ramp(prm, (int)dtype, vec, prm.ay.nseg * prm.ax.nseg, (int)max_pieces,
+    int small = 0;
+    for (int g : {0, 1, 3, 4}) small += prm.ycnt[g / tb::RAMP_MAXCOVER] * prm.xcnt[g % tb::RAMP_MAXCOVER];
+    cudaError_t e = tb::launch_ramp(prm, (int)dtype, vec, small, prm.ay.nseg * prm.ax.nseg - small, (int)max_pieces,
                                     reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return TB_OK;

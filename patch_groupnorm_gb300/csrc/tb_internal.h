@@ -286,7 +286,10 @@ static_assert(sizeof(RampParams) <= 32000, "kernel parameter block too large");
 
 int ramp_block();
 int ramp_smem();
-cudaError_t launch_ramp(const RampParams& p, int dtype, int vec, int grid_x, int grid_y, cudaStream_t s);
+// Launches the rectangles of at most 2 x 2 tiles (grid_small of them) and,
+// if any, those with 3 tiles along an axis (grid_large).
+cudaError_t launch_ramp(const RampParams& p, int dtype, int vec, int grid_small, int grid_large, int grid_y,
+                        cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Patchify split / patch gather

@@ -546,12 +546,17 @@ __device__ __forceinline__ void run_rect_vec(const RampParams& p, int sy, int sx
     }
 }
 
-#ifndef TB_RAMP_GROUP_ORDER
-#define TB_RAMP_GROUP_ORDER 1
+#ifndef TB_RAMP_MIN_CTAS_2
+#define TB_RAMP_MIN_CTAS_2 4
 #endif
 
-template <int DT, int VEC>
-__global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_constant__ RampParams p) {
+// MAXC = 2: the rectangles covered by at most 2 x 2 tiles; MAXC = 3: those
+// with 3 tiles along an axis (a separate, larger kernel launched only when
+// such rectangles exist, so the common one keeps fewer registers and less
+// code).
+template <int DT, int VEC, int MAXC>
+__global__ void __launch_bounds__(RAMP_BLOCK, MAXC == 2 ? TB_RAMP_MIN_CTAS_2 : 3)
+    ramp_kernel(const __grid_constant__ RampParams p) {
     extern __shared__ __align__(16) unsigned char s_ring[];
     __shared__ float s_wy[RAMP_WY_CAP * RAMP_MAXCOVER];
     __shared__ float s_wx[RAMP_WX_CAP * 8 * RAMP_MAXCOVER];
@@ -563,21 +568,25 @@ __global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_consta
     // group of equal (height cover, width cover), so that CTAs dispatched
     // together mostly run one code path (fewer instruction-cache misses).
     int sy, sx;
-#if TB_RAMP_GROUP_ORDER
     {
-        const int bx = (int)blockIdx.x;
-        int g = 0;
-        while (g + 1 < RAMP_MAXCOVER * RAMP_MAXCOVER && p.group_start[g + 1] <= bx) ++g;
+        constexpr int NG = MAXC == 2 ? 4 : 5;
+        constexpr int groups[2][5] = {{0, 1, 3, 4, 0}, {2, 5, 6, 7, 8}};
+        int idx = (int)blockIdx.x, g = -1;
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+            const int gq = groups[MAXC - 2][q];
+            const int cnt = p.ycnt[gq / RAMP_MAXCOVER] * p.xcnt[gq % RAMP_MAXCOVER];
+            if (g < 0) {
+                if (idx < cnt) g = gq;
+                else idx -= cnt;
+            }
+        }
+        if (g < 0) return;
         const int gy = g / RAMP_MAXCOVER, gx = g - gy * RAMP_MAXCOVER;
-        const int idx = bx - p.group_start[g];
         const int iy = idx / p.xcnt[gx];
         sy = p.yseg[gy][iy];
         sx = p.xseg[gx][idx - iy * p.xcnt[gx]];
     }
-#else
-    sy = (int)blockIdx.x / p.ax.nseg;
-    sx = (int)blockIdx.x % p.ax.nseg;
-#endif
     const int rem = (int)blockIdx.y;
     const int flat = (int)p.planes * p.ay.seg_len[sy];
     const int fbeg = rem * p.rows_per_piece[sx];
@@ -620,32 +629,46 @@ __global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_consta
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(s_ring);
     if constexpr (VEC * RElt<DT>::BYTES == 16) {
 #define TB_RECT(CY_, CX_) run_rect_vec<CY_, CX_, DT>(p, sy, sx, fbeg, fend, ring, s_wy, wy_table, s_wx, wx_table)
-        switch (cy * 4 + cx) {
-            case 5: TB_RECT(1, 1); break;
-            case 6: TB_RECT(1, 2); break;
-            case 7: TB_RECT(1, 3); break;
-            case 9: TB_RECT(2, 1); break;
-            case 10: TB_RECT(2, 2); break;
-            case 11: TB_RECT(2, 3); break;
-            case 13: TB_RECT(3, 1); break;
-            case 14: TB_RECT(3, 2); break;
-            case 15: TB_RECT(3, 3); break;
-            default: break;
+        if constexpr (MAXC == 2) {
+            switch (cy * 4 + cx) {
+                case 5: TB_RECT(1, 1); break;
+                case 6: TB_RECT(1, 2); break;
+                case 9: TB_RECT(2, 1); break;
+                case 10: TB_RECT(2, 2); break;
+                default: break;
+            }
+        } else {
+            switch (cy * 4 + cx) {
+                case 7: TB_RECT(1, 3); break;
+                case 11: TB_RECT(2, 3); break;
+                case 13: TB_RECT(3, 1); break;
+                case 14: TB_RECT(3, 2); break;
+                case 15: TB_RECT(3, 3); break;
+                default: break;
+            }
         }
 #undef TB_RECT
     } else {
-        switch (cy * 4 + cx) {
-            case 5: run_rect<1, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-            case 6: run_rect<1, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-            case 7: run_rect<1, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-            case 9: run_rect<2, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-            case 10: run_rect<2, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-            case 11: run_rect<2, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-            case 13: run_rect<3, 1, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-            case 14: run_rect<3, 2, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-            case 15: run_rect<3, 3, DT, VEC>(p, sy, sx, fbeg, fend, ring); break;
-            default: break;
+#define TB_RECT(CY_, CX_) run_rect<CY_, CX_, DT, VEC>(p, sy, sx, fbeg, fend, ring)
+        if constexpr (MAXC == 2) {
+            switch (cy * 4 + cx) {
+                case 5: TB_RECT(1, 1); break;
+                case 6: TB_RECT(1, 2); break;
+                case 9: TB_RECT(2, 1); break;
+                case 10: TB_RECT(2, 2); break;
+                default: break;
+            }
+        } else {
+            switch (cy * 4 + cx) {
+                case 7: TB_RECT(1, 3); break;
+                case 11: TB_RECT(2, 3); break;
+                case 13: TB_RECT(3, 1); break;
+                case 14: TB_RECT(3, 2); break;
+                case 15: TB_RECT(3, 3); break;
+                default: break;
+            }
         }
+#undef TB_RECT
     }
 }
 
@@ -654,24 +677,39 @@ __global__ void __launch_bounds__(RAMP_BLOCK, 3) ramp_kernel(const __grid_consta
 int ramp_block() { return RAMP_BLOCK; }
 int ramp_smem() { return RAMP_SLOTS * RAMP_BLOCK * 16; }
 
-cudaError_t launch_ramp(const RampParams& p, int dtype, int vec, int grid_x, int grid_y, cudaStream_t s) {
-    void (*fn)(const RampParams);
-    switch (dtype) {
-        case F32: fn = vec > 1 ? ramp_kernel<F32, 4> : ramp_kernel<F32, 1>; break;
-        case F16: fn = vec > 1 ? ramp_kernel<F16, 8> : ramp_kernel<F16, 1>; break;
-        default: fn = vec > 1 ? ramp_kernel<BF16, 8> : ramp_kernel<BF16, 1>; break;
+cudaError_t launch_ramp(const RampParams& p, int dtype, int vec, int grid_small, int grid_large, int grid_y,
+                        cudaStream_t s) {
+    for (int big = 0; big < 2; ++big) {
+        const int grid_x = big ? grid_large : grid_small;
+        if (grid_x <= 0) continue;
+        void (*fn)(const RampParams);
+        if (big) {
+            switch (dtype) {
+                case F32: fn = vec > 1 ? ramp_kernel<F32, 4, 3> : ramp_kernel<F32, 1, 3>; break;
+                case F16: fn = vec > 1 ? ramp_kernel<F16, 8, 3> : ramp_kernel<F16, 1, 3>; break;
+                default: fn = vec > 1 ? ramp_kernel<BF16, 8, 3> : ramp_kernel<BF16, 1, 3>; break;
+            }
+        } else {
+            switch (dtype) {
+                case F32: fn = vec > 1 ? ramp_kernel<F32, 4, 2> : ramp_kernel<F32, 1, 2>; break;
+                case F16: fn = vec > 1 ? ramp_kernel<F16, 8, 2> : ramp_kernel<F16, 1, 2>; break;
+                default: fn = vec > 1 ? ramp_kernel<BF16, 8, 2> : ramp_kernel<BF16, 1, 2>; break;
+            }
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid_x, (unsigned)grid_y, 1);
+        cfg.blockDim = dim3(RAMP_BLOCK, 1, 1);
+        cfg.dynamicSmemBytes = vec > 1 ? (size_t)ramp_smem() : 0;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
+        if (e != cudaSuccess) return e;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid_x, (unsigned)grid_y, 1);
-    cfg.blockDim = dim3(RAMP_BLOCK, 1, 1);
-    cfg.dynamicSmemBytes = vec > 1 ? (size_t)ramp_smem() : 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, p);
+    return cudaSuccess;
 }
 
 }  // namespace tb
