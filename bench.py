@@ -19,8 +19,11 @@ The JSON line also carries:
               the DRAM traffic of the last ncu capture of the same kernel
               source (null if the source changed since);
   kernels     every kernel on its own workload: rotating buffer sets (no
-              L2 reuse), launches replayed from a CUDA graph, CUDA events;
-              and one launch at a time after an L2 flush (us_single);
+              L2 reuse), launches replayed from a CUDA graph, CUDA events
+              (us); the single-launch duration under ncu recorded in
+              profiles/single_launch.txt for the current kernel source
+              (us_ncu_single); and one launch at a time after an L2 flush,
+              GPU-side launch included (us_single);
   cpu_baseline  the CPU oracle timed on this host: whole steps for about 10 s
               on all cores (one plane per thread) and 10 s single-threaded.
 
@@ -132,6 +135,23 @@ def profiled_traffic(kernel_key, src_path):
     except OSError:
         pass
     return None, None
+
+
+def profiled_single_us(kernel_key):
+    """Median single-launch duration under ncu recorded in
+    profiles/single_launch.txt for this kernel/workload, while the kernel
+    source still matches the capture; else None."""
+    p = os.path.join(ROOT, "profiles", "single_launch.txt")
+    try:
+        for line in open(p):
+            if line.startswith("#") or not line.strip():
+                continue
+            f = line.split()
+            if f[0] == kernel_key:
+                return float(f[1]) if f[3] == source_digest(os.path.join(ROOT, f[2])) else None
+    except OSError:
+        pass
+    return None
 
 
 class ClockSampler:
@@ -471,10 +491,13 @@ def per_kernel(torch, tb, W, dev, peak, reps, only=None):
         del g
         ms1 = single_ms(launch_set, nsets)
         gbs1 = nbytes / (ms1 * 1e-3) / 1e9
+        ncu_us = profiled_single_us("%s/%s" % (name, workload))
         res.append({"kernel": name, "workload": workload, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
-                    "frac_of_peak": round(gbs / peak, 4), "us_single": round(ms1 * 1e3, 2),
-                    "GB/s_single": round(gbs1, 1), "frac_single": round(gbs1 / peak, 4), "bytes": nbytes,
-                    "sets": nsets})
+                    "frac_of_peak": round(gbs / peak, 4),
+                    "us_ncu_single": ncu_us,
+                    "frac_ncu_single": round(nbytes / (ncu_us * 1e-6) / 1e9 / peak, 4) if ncu_us else None,
+                    "us_single": round(ms1 * 1e3, 2), "GB/s_single": round(gbs1, 1),
+                    "frac_single": round(gbs1 / peak, 4), "bytes": nbytes, "sets": nsets})
 
     def nsets_for(nbytes):
         return max(2, math.ceil(3 * L2_BYTES / nbytes) + 1)
