@@ -24,7 +24,8 @@
 // their own record and the unit's remaining records get count 0, so the
 // records describe themselves (the apply step merges every record with
 // elements, whatever split produced it).  Each thread streams 16-byte chunks through a
-// ring of cp.async slots, seven ahead.  For fp16 / bf16 it sums x - K and
+// ring of cp.async slots, seven ahead (range checks only in the last groups
+// of its run).  For fp16 / bf16 it sums x - K and
 // (x - K)^2 over groups of 8 chunks (64 elements) on packed fp32 pairs, K
 // being the group's first element -- differences and squares of 16-bit
 // values are nearly always exact in fp32, and the shift keeps
@@ -246,6 +247,45 @@ __device__ __forceinline__ uint4 lds16(uint32_t saddr) {
     return v;
 }
 
+// Groups whose chunks and fetches ahead are all in range skip the range
+// checks (0: every group checks, as the tail of a thread's run does).
+#ifndef TB_GN_FAST_GROUPS
+#define TB_GN_FAST_GROUPS 1
+#endif
+
+// The shifted sums of the group of chunks k0 .. k0 + STATS_GROUP - 1 from the
+// thread's cp.async ring (the group starts on ring slot 0), each chunk
+// fetching the one STATS_SLOTS - 1 ahead at `next`.  CHECKED: only the chunks
+// below cnt, and only the fetches below cnt (the tail of a thread's run);
+// otherwise the whole group and all its fetches are known to be in range.
+template <int DT, bool CHECKED>
+__device__ __forceinline__ void stats_group(uint32_t ring, const uint4*& next, int k0, int cnt, unsigned long long& s1,
+                                            unsigned long long& s2, unsigned long long& k2, float& K) {
+    constexpr uint32_t SLOT = STATS_BLOCK * 16u;
+#pragma unroll
+    for (int u = 0; u < STATS_GROUP; ++u) {
+        if (!CHECKED || k0 + u < cnt) {
+            if (!CHECKED || k0 + u + STATS_SLOTS - 1 < cnt)
+                cp_async16(ring + ((u + STATS_SLOTS - 1) % STATS_SLOTS) * SLOT, next);
+            next += STATS_BLOCK;
+            cp_async_commit();
+            cp_async_wait<STATS_SLOTS - 1>();
+            const uint4 v = lds16(ring + (u % STATS_SLOTS) * SLOT);
+            if (u == 0) {
+                K = GElt<DT>::to_f(v.x);
+                const unsigned long long kb = __float_as_uint(K);
+                k2 = kb | (kb << 32);
+                s1 = 0;
+                s2 = 0;
+            }
+            shifted_acc<DT>(v.x, k2, s1, s2);
+            shifted_acc<DT>(v.y, k2, s1, s2);
+            shifted_acc<DT>(v.z, k2, s1, s2);
+            shifted_acc<DT>(v.w, k2, s1, s2);
+        }
+    }
+}
+
 template <int DT, bool VECTOR>
 __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_constant__ GnStatsParams p) {
     constexpr int VEC = 16 / GElt<DT>::BYTES;
@@ -298,29 +338,14 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
             float K = 0.f;
             const uint4* next = src + first + (int64_t)(STATS_SLOTS - 1) * STATS_BLOCK;  // chunk k + SLOTS - 1
             for (int k0 = 0; k0 < cnt; k0 += STATS_GROUP) {
-                const int m = min(STATS_GROUP, cnt - k0);
-#pragma unroll
-                for (int u = 0; u < STATS_GROUP; ++u) {
-                    if (u < m) {
-                        if (k0 + u + STATS_SLOTS - 1 < cnt)
-                            cp_async16(ring + ((u + STATS_SLOTS - 1) % STATS_SLOTS) * SLOT, next);
-                        next += STATS_BLOCK;
-                        cp_async_commit();
-                        cp_async_wait<STATS_SLOTS - 1>();
-                        const uint4 v = lds16(ring + (u % STATS_SLOTS) * SLOT);
-                        if (u == 0) {
-                            K = GElt<DT>::to_f(v.x);
-                            const unsigned long long kb = __float_as_uint(K);
-                            k2 = kb | (kb << 32);
-                            s1 = 0;
-                            s2 = 0;
-                        }
-                        shifted_acc<DT>(v.x, k2, s1, s2);
-                        shifted_acc<DT>(v.y, k2, s1, s2);
-                        shifted_acc<DT>(v.z, k2, s1, s2);
-                        shifted_acc<DT>(v.w, k2, s1, s2);
-                    }
+                if (TB_GN_FAST_GROUPS && k0 + STATS_GROUP + STATS_SLOTS - 1 <= cnt) {
+                    // a whole group whose fetches ahead are all in range: no checks
+                    stats_group<DT, false>(ring, next, k0, cnt, s1, s2, k2, K);
+                    acc = chan_fast(acc, shifted_stat(s1, s2, K, (float)(STATS_GROUP * VEC)));
+                    continue;
                 }
+                const int m = min(STATS_GROUP, cnt - k0);
+                stats_group<DT, true>(ring, next, k0, cnt, s1, s2, k2, K);
                 // merging into the empty triple of the first group is exact
                 acc = chan_fast(acc, shifted_stat(s1, s2, K, (float)(m * VEC)));
             }

@@ -97,6 +97,42 @@ def test_partials_match_oracle(tbl, dtype):
     assert np.abs(M2 / om2.reshape(-1) - 1).max() <= 2e-5
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_ragged_patches_with_an_empty_one_in_the_middle(tbl, dtype):
+    # 768 units of 240-272 chunks (16 bytes) over ragged patches, one of them
+    # empty and between the others: every record of the empty patch's units
+    # is empty, the counts of each unit add up, and the pooled statistics and
+    # outputs match the oracle.
+    vec = 4 if dtype == "f32" else 8
+    heights = [30, 0, 34, 32, 33, 31]
+    g = torch.Generator().manual_seed(240)
+    x = torch.randn(4, 64, sum(heights), 32 * 8 // vec, generator=g, dtype=torch.float64) * 1.3
+    parts = _split(x, 2, heights)
+    parts = [(p + m).to(TORCH[dtype]) for p, m in zip(parts, [-2.0, 0.0, 2.5, -1.0, 1.0, 3.0])]
+    G = 32
+    gamma = (1 + 0.1 * torch.randn(64, generator=g, dtype=torch.float64)).to(TORCH[dtype])
+    beta = (0.1 * torch.randn(64, generator=g, dtype=torch.float64)).to(TORCH[dtype])
+    outs, part = run_gpu(tbl, parts, G, gamma, beta, 1e-6, True)
+    with np.errstate(over="ignore"):
+        assert check_outputs(outs, parts, gamma, beta, G, 1e-6, True, dtype) <= 1.0
+    part = part.view(-1, tbl.TB_GN_PARTS, 2).numpy()
+    cnt = part[..., 0]
+    packed = np.ascontiguousarray(part[..., 1]).view(np.float32).reshape(part.shape[0], tbl.TB_GN_PARTS, 2)
+    assert ((cnt > 0) | ((packed[..., 0] == 0) & (packed[..., 1] == 0))).all()
+    oc, om, om2 = GN.patch_partials([_f64(p) for p in parts], G)
+    assert np.array_equal(cnt.sum(axis=1), oc.reshape(-1))
+    assert (cnt.reshape(6, -1)[1] == 0).all()
+    c64 = cnt.astype(np.float64)
+    mean, m2 = packed[..., 0].astype(np.float64), packed[..., 1].astype(np.float64)
+    n = c64.sum(axis=1)
+    keep = n > 0
+    mu = (c64 * mean).sum(axis=1)[keep] / n[keep]
+    M2 = (m2[keep] + c64[keep] * (mean[keep] - mu[:, None]) ** 2).sum(axis=1)
+    om, om2 = om.reshape(-1)[keep], om2.reshape(-1)[keep]
+    assert np.abs(mu - om).max() <= 2e-5 * np.maximum(1, np.abs(om)).max()
+    assert np.abs(M2 / om2 - 1).max() <= 2e-5
+
+
 def test_stats_deterministic(tbl):
     patches, _, _ = synth.groupnorm_patches(4, (1, 64, 96, 96), 3, 4, (-3, -1, 1, 3), "bf16")
     _, a = run_gpu(tbl, patches, 32, None, None, 1e-6, False)
