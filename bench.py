@@ -154,6 +154,89 @@ def profiled_single_us(kernel_key):
     return None
 
 
+# A child process that reads the SM clock and the clock-event reasons
+# through NVML (the driver's library, by ctypes: read-only queries) every
+# half millisecond, so a timed region of a millisecond still holds samples.
+# It prints "ready" once NVML answers, keeps its samples in memory and, when
+# terminated, prints one line per sample: wall time, SM MHz, max SM MHz,
+# reasons bitmask.
+NVML_CHILD = r"""
+import ctypes, signal, sys, time
+uuid = sys.argv[1].encode()
+nv = ctypes.CDLL("libnvidia-ml.so.1")
+if nv.nvmlInit_v2() != 0:
+    sys.exit(1)
+h = ctypes.c_void_p()
+if nv.nvmlDeviceGetHandleByUUID(uuid, ctypes.byref(h)) != 0:
+    sys.exit(1)
+try:
+    reasons_fn = nv.nvmlDeviceGetCurrentClocksEventReasons
+except AttributeError:
+    reasons_fn = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+mx = ctypes.c_uint()
+nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+sm, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+stop = []
+signal.signal(signal.SIGTERM, lambda *a: stop.append(1))
+print("ready", flush=True)
+rows = []
+while not stop:
+    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and reasons_fn(h, ctypes.byref(rs)) == 0:
+        rows.append((time.time(), sm.value, mx.value, rs.value))
+    time.sleep(0.0005)
+sys.stdout.write("".join("%.6f %d %d %d\n" % r for r in rows))
+sys.stdout.flush()
+"""
+
+
+class NvmlSampler:
+    """SM clock and clock-event reasons every 0.5 ms from a child process
+    (NVML through ctypes); no rows if NVML cannot be used."""
+    # NVML clock-event reason bits (nvml.h)
+    BITS = (("hw", 0x8), ("hw_thermal", 0x40), ("sw_thermal", 0x20), ("sw_power", 0x4))
+
+    def __init__(self, gpu_uuid):
+        self.proc = None
+        self.first = ""
+        if gpu_uuid is None:
+            return
+        try:
+            self.proc = subprocess.Popen([sys.executable, "-c", NVML_CHILD, gpu_uuid], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+
+    def wait_ready(self, timeout=3.0):
+        """Waits (at most `timeout` s) for the child's first sample."""
+        if self.proc is None:
+            return
+        import select
+        if select.select([self.proc.stdout], [], [], timeout)[0]:
+            self.first = self.proc.stdout.readline()
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in (self.first + out).splitlines():
+            f = line.split()
+            if len(f) != 4:
+                continue
+            bits = int(f[3])
+            row = dict(t=float(f[0]), sm=float(f[1]), sm_max=float(f[2]))
+            for k, b in self.BITS:
+                row[k] = "Active" if bits & b else "Not Active"
+            rows.append(row)
+        return rows
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
     Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -195,11 +278,11 @@ class ClockSampler:
         return rows
 
     @staticmethod
-    def summarise(rows, t0, t1):
+    def summarise(rows, t0, t1, margin=0.05, source="nvidia-smi every 100 ms"):
         if not rows:
             return None
-        inside = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05]
-        window = "timed region"
+        inside = [r for r in rows if t0 - margin <= r["t"] <= t1 + margin]
+        window = "timed region" if margin == 0 else "timed region +- %.0f ms" % (margin * 1e3)
         if not inside:
             # the region was shorter than the sampling period: nearest samples
             mid = 0.5 * (t0 + t1)
@@ -212,7 +295,8 @@ class ClockSampler:
                 if r[k].lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(r["sm"] for r in inside), "sm_max_mhz": max(r["sm_max"] for r in inside),
-                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+                "sm_min_mhz": min(r["sm"] for r in inside), "reasons": sorted(reasons), "samples": len(inside),
+                "window": window, "source": source}
 
 
 # ---------------------------------------------------------------------------
@@ -342,7 +426,9 @@ def run_ours(args):
     except Exception:
         gpu_id = None
     sampler = ClockSampler(gpu_id)
-    time.sleep(0.3)  # the sampler's first reading
+    fine = NvmlSampler(gpu_id)
+    time.sleep(0.3)  # the samplers' first readings
+    fine.wait_ready()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -363,6 +449,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     time.sleep(0.15)
+    fine_rows = fine.stop()
     rows = sampler.stop()
     ms = max_over_ranks(torch, dist, world, e0.elapsed_time(e1), dev)
     ms_per_step = ms / args.steps
@@ -370,7 +457,10 @@ def run_ours(args):
     value = whole_job_gbs(alg_bytes, ms_per_step, world)
     peak, peak_kind = measured_peaks()
     mpix = w.B * H * Wd / (ms_per_step * 1e-3) / 1e6 * world
-    clocks = ClockSampler.summarise(rows, t_wall0, t_wall1)
+    if any(t_wall0 <= r["t"] <= t_wall1 for r in fine_rows):
+        clocks = ClockSampler.summarise(fine_rows, t_wall0, t_wall1, 0.0, "NVML every 0.5 ms (read-only queries)")
+    else:
+        clocks = ClockSampler.summarise(rows, t_wall0, t_wall1)
 
     # end to end through the C ABI with host buffers: every step copies its
     # tiles in from pinned host memory and its image back out.  The tiles sit
