@@ -70,7 +70,7 @@ constexpr int STATS_SLOTS = TB_GN_STATS_SLOTS;  // cp.async ring slots per threa
 constexpr int STATS_GROUP = TB_GN_STATS_GROUP;  // 16-bit chunks per shifted-sum group
 constexpr int APPLY_BLOCK = 128;
 #ifndef TB_GN_APPLY_CPT
-#define TB_GN_APPLY_CPT 8
+#define TB_GN_APPLY_CPT 16
 #endif
 constexpr int APPLY_CPT = TB_GN_APPLY_CPT;  // 16-byte chunks per thread per segment
 
