@@ -585,7 +585,9 @@ def run_ours(args):
                        "algorithmic_bytes_per_step": alg_bytes,
                        "l2": "3 rotating input/output sets (%.0f MB) > 129 MB L2; no flush" % (
                            nsets * alg_bytes / 1e6),
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+                       "parallelism": "dp%d" % world if world > 1 else "single GPU",
+                       "sharding": "every rank stitches its own batch of %d images (independent images: no "
+                                   "exchange, no collective on the data path)" % w.B},
             "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps, "roofline": roofline,
             "cpu_baseline": cpu, "kernels": kernels,
         }
