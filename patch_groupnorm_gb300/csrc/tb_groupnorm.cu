@@ -525,6 +525,46 @@ __device__ __forceinline__ float act(float x, float a, float b) {
     }
 }
 
+// act() on a pair of elements: the fp32 operations in packed pairs
+// (fma/mul/add.rn.f32x2 round each lane exactly as the scalar instructions
+// do, so the results are the same bits), the special-function ops per lane.
+#ifndef TB_GN_APPLY_PACKED
+#define TB_GN_APPLY_PACKED 1
+#endif
+__device__ __forceinline__ unsigned long long pack2f(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2f(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+template <int SILU>
+__device__ __forceinline__ void act2(float& lo, float& hi, unsigned long long a2, unsigned long long b2) {
+    if constexpr (!TB_GN_APPLY_PACKED) {
+        float a, b, a1, b1;
+        unpack2f(a2, a, a1);
+        unpack2f(b2, b, b1);
+        lo = act<SILU>(lo, a, b);
+        hi = act<SILU>(hi, a1, b1);
+        return;
+    }
+    unsigned long long z;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(z) : "l"(pack2f(lo, hi)), "l"(a2), "l"(b2));
+    if constexpr (SILU) {
+        unsigned long long t, d, y;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(z), "l"(pack2f(-1.4426950408889634f, -1.4426950408889634f)));
+        float tl, th;
+        unpack2f(t, tl, th);
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2f(ex2_ftz(tl), ex2_ftz(th))), "l"(pack2f(1.0f, 1.0f)));
+        float dl, dh;
+        unpack2f(d, dl, dh);
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(z), "l"(pack2f(rcp_ftz(dl), rcp_ftz(dh))));
+        z = y;
+    }
+    unpack2f(z, lo, hi);
+}
+
 template <int DT, bool VECTOR, int SILU>
 __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_constant__ GnApplyParams p) {
     constexpr int VEC = VECTOR ? 16 / GElt<DT>::BYTES : 1;
@@ -559,24 +599,26 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
             if (idx < nchunk) v[q] = __ldcs(src + idx);
         }
         const float2 ab = channel_affine<DT>(p, n, g, c);
-        const float a = ab.x, b = ab.y;
+        const unsigned long long a2 = pack2f(ab.x, ab.x), b2 = pack2f(ab.y, ab.y);
 #pragma unroll
         for (int q = 0; q < APPLY_CPT; ++q) {
             const int idx = threadIdx.x + q * APPLY_BLOCK;
             if (idx >= nchunk) continue;
             uint4 o;
             if constexpr (GElt<DT>::BYTES == 4) {
-                o.x = __float_as_uint(act<SILU>(__uint_as_float(v[q].x), a, b));
-                o.y = __float_as_uint(act<SILU>(__uint_as_float(v[q].y), a, b));
-                o.z = __float_as_uint(act<SILU>(__uint_as_float(v[q].z), a, b));
-                o.w = __float_as_uint(act<SILU>(__uint_as_float(v[q].w), a, b));
+                float x0 = __uint_as_float(v[q].x), x1 = __uint_as_float(v[q].y);
+                float x2 = __uint_as_float(v[q].z), x3 = __uint_as_float(v[q].w);
+                act2<SILU>(x0, x1, a2, b2);
+                act2<SILU>(x2, x3, a2, b2);
+                o = make_uint4(__float_as_uint(x0), __float_as_uint(x1), __float_as_uint(x2), __float_as_uint(x3));
             } else {
                 uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     float lo, hi;
                     GElt<DT>::unpack(w[k], lo, hi);
-                    w[k] = GElt<DT>::pack(act<SILU>(lo, a, b), act<SILU>(hi, a, b));
+                    act2<SILU>(lo, hi, a2, b2);
+                    w[k] = GElt<DT>::pack(lo, hi);
                 }
                 o = make_uint4(w[0], w[1], w[2], w[3]);
             }
