@@ -1,6 +1,7 @@
 """CUDA-graph replay of the sharded-decode steps (Patchify split, PatchGroupNorm
-statistics and normalisation, patch gather) and of the ramp stitch, captured
-once and replayed with new contents at the same addresses.  Every call passes
+statistics and normalisation, patch gather), of the ramp stitch and of the
+row-sharded stitch (halo pack and the ranks' stitches), captured once and
+replayed with new contents at the same addresses.  Every call passes
 its parameters by value, so each replay must reproduce the oracle's result
 for the inputs present at replay time."""
 import numpy as np
@@ -88,3 +89,49 @@ def test_ramp_stitch_replays_with_new_inputs(tbl):
                                ay.tile_extent, ax.tile_extent, (ay.out_extent, ax.out_extent), ay.zero, ay.ramp,
                                ax.zero, ax.ramp)
         assert _within_one_ulp(out, exact, "bf16")
+
+
+def test_row_sharded_stitch_replays_with_new_inputs(tbl):
+    # two ranks' shares of a row-sharded stitch run one after the other on
+    # this GPU: rank 0 packs the band its last tile row lends (halo pack) into
+    # the buffer the exchange would deliver to rank 1, and each rank stitches
+    # its own tile rows; pack and stitches captured once, replayed with new
+    # tiles, must equal the unsharded stitch of those tiles bit for bit
+    from oracle.geometry import axis_layout
+    ay, ax = tbl.Axis(48, 16, 0.25, 8), tbl.Axis(40, 16, 0.25, 8)
+    ly = axis_layout(48, 16, 0.25, 8)
+    lx = axis_layout(40, 16, 0.25, 8)
+    B, C = 1, 3
+    tiles = [[torch.empty((B, C, hy, wx), dtype=torch.bfloat16, device="cuda") for wx in lx.extents]
+             for hy in ly.extents]
+    lays = [tbl.tb_stitch_shard_layout(None, ay, ax, B, C, 2, r) for r in range(2)]
+    assert lays[0].send_elems > 0 and lays[1].halo_elems == lays[0].send_elems
+    band = torch.empty(lays[0].send_elems, dtype=torch.bfloat16, device="cuda")
+    outs = [torch.empty((B, C, lay.out_rows, lx.out_extent), dtype=torch.bfloat16, device="cuda") for lay in lays]
+    whole = torch.empty((B, C, ly.out_extent, lx.out_extent), dtype=torch.bfloat16, device="cuda")
+
+    def ranks():
+        l0, l1 = lays
+        tbl.tb_stitch_halo_pack(tiles[l0.row_end - 1], None, ay, ax, l0.row_end - 1, band)
+        tbl.tb_stitch2d_shard(tiles[l0.row_begin:l0.row_end], None, ay, ax, l0.row_begin, l0.row_end, outs[0])
+        tbl.tb_stitch2d_shard(tiles[l1.row_begin:l1.row_end], band, ay, ax, l1.row_begin, l1.row_end, outs[1])
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ranks()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ranks()
+    rng = np.random.default_rng(9)
+    for _ in range(3):
+        for row in tiles:
+            for t in row:
+                t.copy_(torch.from_numpy(rng.uniform(-1, 1, tuple(t.shape))).to(torch.bfloat16))
+        band.fill_(float("nan"))
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        tbl.tb_stitch2d(tiles, ay, ax, whole)
+        torch.cuda.synchronize()
+        assert torch.equal(torch.cat(outs, dim=2).view(torch.int16), whole.view(torch.int16))
