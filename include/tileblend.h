@@ -28,10 +28,11 @@
  *     an invalid call returns an error status and launches nothing.  No call
  *     aborts, throws or prints.
  *   - Tensors are dense, contiguous, row-major (last dimension fastest).
- *   - Kernel parameters are passed by value, so the stitch, ramp, Patchify,
- *     gather, halo-pack and two-call GroupNorm calls can be captured into a
- *     CUDA graph and replayed with new tensor contents at the same addresses
- *     (tested).
+ *   - Kernel parameters are passed by value.  Captured into a CUDA graph
+ *     and replayed with new tensor contents at the same addresses (tested):
+ *     tb_stitch2d, tb_stitch2d_ramp, tb_patchify, tb_gather_patches,
+ *     tb_stitch_halo_pack with tb_stitch2d_shard, and tb_patch_gn_stats with
+ *     tb_patch_gn_apply.
  */
 #ifndef TILEBLEND_H
 #define TILEBLEND_H
