@@ -258,15 +258,23 @@ __device__ __forceinline__ uint4 lds16(uint32_t saddr) {
 // fetching the one STATS_SLOTS - 1 ahead at `next`.  CHECKED: only the chunks
 // below cnt, and only the fetches below cnt (the tail of a thread's run);
 // otherwise the whole group and all its fetches are known to be in range.
+// One 16-byte chunk of the unit [unit, unit + nv) into a ring slot; the
+// bounds-checked build checks the address first.
+__device__ __forceinline__ void stats_fetch(uint32_t dst, const uint4* at, const uint4* unit, int64_t nv,
+                                            uint32_t* status) {
+    if (in_bounds(at, 16, unit, nv * 16, status)) cp_async16(dst, at);
+}
+
 template <int DT, bool CHECKED>
 __device__ __forceinline__ void stats_group(uint32_t ring, const uint4*& next, int k0, int cnt, unsigned long long& s1,
-                                            unsigned long long& s2, unsigned long long& k2, float& K) {
+                                            unsigned long long& s2, unsigned long long& k2, float& K,
+                                            const uint4* unit, int64_t nv, uint32_t* status) {
     constexpr uint32_t SLOT = STATS_BLOCK * 16u;
 #pragma unroll
     for (int u = 0; u < STATS_GROUP; ++u) {
         if (!CHECKED || k0 + u < cnt) {
             if (!CHECKED || k0 + u + STATS_SLOTS - 1 < cnt)
-                cp_async16(ring + ((u + STATS_SLOTS - 1) % STATS_SLOTS) * SLOT, next);
+                stats_fetch(ring + ((u + STATS_SLOTS - 1) % STATS_SLOTS) * SLOT, next, unit, nv, status);
             next += STATS_BLOCK;
             cp_async_commit();
             cp_async_wait<STATS_SLOTS - 1>();
@@ -323,7 +331,7 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
         constexpr uint32_t SLOT = STATS_BLOCK * 16u;
 #pragma unroll
         for (int k = 0; k < STATS_SLOTS - 1; ++k) {
-            if (k < cnt) cp_async16(ring + k * SLOT, src + first + (int64_t)k * STATS_BLOCK);
+            if (k < cnt) stats_fetch(ring + k * SLOT, src + first + (int64_t)k * STATS_BLOCK, src, nv, p.status);
             cp_async_commit();
         }
         if constexpr (GElt<DT>::BYTES == 2) {
@@ -340,12 +348,12 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
             for (int k0 = 0; k0 < cnt; k0 += STATS_GROUP) {
                 if (TB_GN_FAST_GROUPS && k0 + STATS_GROUP + STATS_SLOTS - 1 <= cnt) {
                     // a whole group whose fetches ahead are all in range: no checks
-                    stats_group<DT, false>(ring, next, k0, cnt, s1, s2, k2, K);
+                    stats_group<DT, false>(ring, next, k0, cnt, s1, s2, k2, K, src, nv, p.status);
                     acc = chan_fast(acc, shifted_stat(s1, s2, K, (float)(STATS_GROUP * VEC)));
                     continue;
                 }
                 const int m = min(STATS_GROUP, cnt - k0);
-                stats_group<DT, true>(ring, next, k0, cnt, s1, s2, k2, K);
+                stats_group<DT, true>(ring, next, k0, cnt, s1, s2, k2, K, src, nv, p.status);
                 // merging into the empty triple of the first group is exact
                 acc = chan_fast(acc, shifted_stat(s1, s2, K, (float)(m * VEC)));
             }
@@ -353,7 +361,8 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
             for (int k = 0; k < cnt; ++k) {
                 const int ahead = k + STATS_SLOTS - 1;
                 if (ahead < cnt)
-                    cp_async16(ring + (ahead % STATS_SLOTS) * SLOT, src + first + (int64_t)ahead * STATS_BLOCK);
+                    stats_fetch(ring + (ahead % STATS_SLOTS) * SLOT, src + first + (int64_t)ahead * STATS_BLOCK, src,
+                                nv, p.status);
                 cp_async_commit();
                 cp_async_wait<STATS_SLOTS - 1>();
                 float x[VEC];
@@ -365,6 +374,7 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
     } else {
         const int64_t e0 = len * rank / parts, e1 = len * (rank + 1) / parts;
         for (int64_t e = e0 + threadIdx.x; e < e1; e += STATS_BLOCK) {
+            if (!index_ok(e >= 0 && e < len, p.status)) continue;
             const float x = load_scalar<DT>(base, e);
             acc = chan(acc, Stat{1.f, x, 0.f});
         }
@@ -388,6 +398,7 @@ __global__ void __launch_bounds__(STATS_BLOCK) gn_stats_kernel(const __grid_cons
         } else {
             count = len * (rank + 1) / parts - len * rank / parts;
         }
+        if (!index_ok(unit < (unsigned)p.P * NG && rank < TB_GN_PARTS, p.status)) return;
         GnPartial* const rec = p.partials + (int64_t)unit * TB_GN_PARTS;
         GnPartial out;
         out.n = count;
@@ -417,7 +428,14 @@ __device__ __forceinline__ void pooled_stats(const GnApplyParams& p, int64_t n, 
     const GnPartial* const unit0 = p.partials + (n * p.G + g) * TB_GN_PARTS;
     auto record = [&](int q, long long& c, float& m, float& m2) {
         const int r = q / TB_GN_PARTS, k = q - r * TB_GN_PARTS;
-        const longlong2 raw = __ldg(reinterpret_cast<const longlong2*>(unit0 + r * set_stride + k));
+        const GnPartial* const at = unit0 + r * set_stride + k;
+        if (!in_bounds(at, sizeof(GnPartial), p.partials, (int64_t)p.R * set_stride * (int64_t)sizeof(GnPartial),
+                       p.status)) {
+            c = 0;
+            m = m2 = 0.f;
+            return;
+        }
+        const longlong2 raw = __ldg(reinterpret_cast<const longlong2*>(at));
         c = raw.x;
         m = __int_as_float((int)(raw.y & 0xffffffffLL));
         m2 = __int_as_float((int)(raw.y >> 32));
@@ -495,8 +513,9 @@ __device__ __forceinline__ float2 channel_affine(const GnApplyParams& p, int64_t
     pooled_stats(p, n, g, mean, rstd);
     mean = __shfl_sync(0xffffffffu, mean, 0);
     rstd = __shfl_sync(0xffffffffu, rstd, 0);
-    const float a = rstd * load_param<DT>(p.gamma, c, 1.f);
-    return make_float2(a, load_param<DT>(p.beta, c, 0.f) - mean * a);
+    const bool c_ok = index_ok(c >= 0 && c < p.C, p.status);
+    const float a = rstd * (c_ok ? load_param<DT>(p.gamma, c, 1.f) : 1.f);
+    return make_float2(a, (c_ok ? load_param<DT>(p.beta, c, 0.f) : 0.f) - mean * a);
 }
 
 // silu(z) = z / (1 + e^-z), with e^-z = 2^(-z log2 e) and the reciprocal
@@ -587,6 +606,8 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
     // parameters only above; patches and partials come from preceding grids
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    // the patch's and its output's extent, for the bounds-checked build
+    const int64_t pbytes = p.N * p.C * S * GElt<DT>::BYTES;
     if constexpr (VECTOR) {
         // S and every row start are multiples of VEC; issue the data loads first
         const uint4* src = reinterpret_cast<const uint4*>(p.patches[pp]) + (row_start + e_begin) / VEC;
@@ -596,7 +617,10 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
 #pragma unroll
         for (int q = 0; q < APPLY_CPT; ++q) {
             const int idx = threadIdx.x + q * APPLY_BLOCK;
-            if (idx < nchunk) v[q] = __ldcs(src + idx);
+            if (idx < nchunk) {
+                if (in_bounds(src + idx, 16, p.patches[pp], pbytes, p.status)) v[q] = __ldcs(src + idx);
+                else v[q] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         const float2 ab = channel_affine<DT>(p, n, g, c);
         const unsigned long long a2 = pack2f(ab.x, ab.x), b2 = pack2f(ab.y, ab.y);
@@ -622,7 +646,7 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
                 }
                 o = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            __stcs(dst + idx, o);
+            if (in_bounds(dst + idx, 16, p.outs[pp], pbytes, p.status)) __stcs(dst + idx, o);
         }
     } else {
         const float2 ab = channel_affine<DT>(p, n, g, c);
@@ -630,6 +654,7 @@ __global__ void __launch_bounds__(APPLY_BLOCK) gn_apply_kernel(const __grid_cons
         const void* src = p.patches[pp];
         void* dst = p.outs[pp];
         for (int64_t e = e_begin + threadIdx.x; e < e_end; e += APPLY_BLOCK) {
+            if (!index_ok(row_start + e >= 0 && (row_start + e) * GElt<DT>::BYTES < pbytes, p.status)) continue;
             const float y = act<SILU>(load_scalar<DT>(src, row_start + e), a, b);
             if constexpr (GElt<DT>::BYTES == 4) {
                 __stcs(reinterpret_cast<float*>(dst) + row_start + e, y);

@@ -743,6 +743,7 @@ tb_status gn_apply(const void* const* patches, void* const* outs, int32_t P, tb_
     prm.eps = eps;
     prm.silu = silu ? 1 : 0;
     prm.aligned = aligned ? 1 : 0;
+    prm.status = debug_status();
     cudaError_t e = tb::launch_gn_apply(prm, (int)dtype, items, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return TB_OK;
@@ -1289,6 +1290,7 @@ TB_API tb_status tb_patch_gn_stats(const void* const* patches, int32_t P, tb_dty
     prm.P = P;
     prm.G = G;
     prm.aligned = aligned ? 1 : 0;
+    prm.status = debug_status();
     const int64_t units = (int64_t)P * N * G;
     int parts = 1;
     s = gn_parts(P, N, C, spatial, G, dtype, &parts);

@@ -376,6 +376,7 @@ struct GnStatsParams {
     int32_t P, G;
     int32_t parts;                // CTAs per (p, n, g) unit: 1 .. TB_GN_PARTS
     int32_t aligned;              // every unit start and length is a multiple of the vector width
+    uint32_t* status;             // bounds-checked build: device status word (else null)
 };
 
 struct GnApplyParams {
@@ -394,6 +395,7 @@ struct GnApplyParams {
     float eps;
     int32_t silu;
     int32_t aligned;                  // every channel row start is 16-byte aligned
+    uint32_t* status;                 // bounds-checked build: device status word (else null)
 };
 
 // Elements per apply work item (one CTA): depends on the element size and

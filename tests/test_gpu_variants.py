@@ -1,11 +1,12 @@
-"""Two other builds of the same library, each run through the GPU parity tests
+"""Other builds of the same library, each run through the GPU parity tests
 of the kernels it changes (in a child pytest whose binding loads that build
 through TILEBLEND_LIB):
 
 * the bounds-checked build (TB_DEBUG_BOUNDS=1): the stitch (both 2D/3D paths
   and the shard calls), the normalised-ramp stitch, the Patchify split and
-  patch gather, and the halo pack check every computed tile index and every
-  address before they read or write it; a check that fails records
+  patch gather, the halo pack and the GroupNorm statistics and apply check
+  every computed tile index, record index and address before they read or
+  write it; a check that fails records
   TB_DEV_OUT_OF_BOUNDS in the device status word (no trap) and skips the
   access.  Every full-size workload must stay bit-exact (or within its
   tolerance) and the word must read 0 at the end (the stitch file's last
@@ -30,7 +31,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 VARIANTS = {
     "debug_bounds": (["TB_DEBUG_BOUNDS=1"], ["tests/test_gpu_patchify.py", "tests/test_gpu_ramp.py",
-                                              "tests/test_gpu_shard.py", "tests/test_gpu_stitch.py"]),
+                                              "tests/test_gpu_shard.py", "tests/test_gpu_groupnorm.py",
+                                              "tests/test_gpu_graph.py", "tests/test_gpu_stitch.py"]),
     "tma": (["TB_STITCH_TMA=1"], ["tests/test_gpu_shard.py", "tests/test_gpu_stitch.py"]),
     "gn_parts3": (["TB_GN_FORCE_PARTS=3"], ["tests/test_gpu_groupnorm.py", "tests/test_zz_no_alloc.py"]),
 }
