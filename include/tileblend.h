@@ -30,9 +30,11 @@
  *   - Tensors are dense, contiguous, row-major (last dimension fastest).
  *   - Kernel parameters are passed by value.  Captured into a CUDA graph
  *     and replayed with new tensor contents at the same addresses (tested):
- *     tb_stitch2d, tb_stitch2d_ramp, tb_patchify, tb_gather_patches,
- *     tb_stitch_halo_pack with tb_stitch2d_shard, and tb_patch_gn_stats with
- *     tb_patch_gn_apply.
+ *     tb_stitch2d, tb_stitch3d, tb_stitch2d_ramp, tb_patchify,
+ *     tb_gather_patches, tb_stitch_halo_pack with tb_stitch2d_shard,
+ *     tb_stitch_halo_pack_frames with tb_stitch3d_shard_frames, and
+ *     tb_patch_gn_stats with tb_patch_gn_apply and with
+ *     tb_patch_gn_apply_gathered.
  */
 #ifndef TILEBLEND_H
 #define TILEBLEND_H

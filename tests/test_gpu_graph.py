@@ -1,7 +1,8 @@
 """CUDA-graph replay of the sharded-decode steps (Patchify split, PatchGroupNorm
-statistics and normalisation, patch gather), of the ramp stitch and of the
-row-sharded stitch (halo pack and the ranks' stitches), captured once and
-replayed with new contents at the same addresses.  Every call passes
+statistics and normalisation, patch gather), of the ramp stitch, of the
+row-sharded stitch (halo pack and the ranks' stitches), of the video stitch
+with its frame-sharded form, and of per-rank statistics with the gathered
+apply, captured once and replayed with new contents at the same addresses.  Every call passes
 its parameters by value, so each replay must reproduce the oracle's result
 for the inputs present at replay time."""
 import numpy as np
@@ -135,3 +136,97 @@ def test_row_sharded_stitch_replays_with_new_inputs(tbl):
         tbl.tb_stitch2d(tiles, ay, ax, whole)
         torch.cuda.synchronize()
         assert torch.equal(torch.cat(outs, dim=2).view(torch.int16), whole.view(torch.int16))
+
+
+def test_video_stitch_and_frame_sharded_stitch_replay_with_new_inputs(tbl):
+    # tb_stitch3d, and two ranks' shares of the same video sharded along the
+    # frames (frame-band pack + each rank's stitch), in one graph; replayed
+    # with new tiles: the stitch equals the oracle and the ranks' outputs
+    # concatenated equal the stitch, bit for bit
+    from oracle.geometry import axis_layout
+    from oracle.stitch import stitch as oracle_stitch
+    from tests.stitch_helpers import to_storage
+    geo = [(17, 8, 0.25, 1), (24, 8, 0.25, 8), (20, 8, 0.25, 8)]
+    at, ay, ax = (tbl.Axis(*a) for a in geo)
+    lt, ly, lx = (axis_layout(*a) for a in geo)
+    B, C = 1, 2
+    tiles = [[[torch.empty((B, C, ft, hy, wx), dtype=torch.bfloat16, device="cuda") for wx in lx.extents]
+              for hy in ly.extents] for ft in lt.extents]
+    whole = torch.empty((B, C, lt.out_extent, ly.out_extent, lx.out_extent), dtype=torch.bfloat16, device="cuda")
+    lays = [tbl.tb_stitch_shard_frames_layout(at, ay, ax, B, C, 2, r) for r in range(2)]
+    assert lays[0].send_elems > 0 and lays[1].halo_elems == lays[0].send_elems
+    band = torch.empty(lays[0].send_elems, dtype=torch.bfloat16, device="cuda")
+    outs = [torch.empty((B, C, lay.out_rows, ly.out_extent, lx.out_extent), dtype=torch.bfloat16, device="cuda")
+            for lay in lays]
+
+    def run():
+        l0, l1 = lays
+        tbl.tb_stitch3d(tiles, at, ay, ax, whole)
+        tbl.tb_stitch_halo_pack_frames(tiles[l0.row_end - 1], at, ay, ax, l0.row_end - 1, band)
+        tbl.tb_stitch3d_shard_frames(tiles[l0.row_begin:l0.row_end], None, at, ay, ax, l0.row_begin, l0.row_end,
+                                     outs[0])
+        tbl.tb_stitch3d_shard_frames(tiles[l1.row_begin:l1.row_end], band, at, ay, ax, l1.row_begin, l1.row_end,
+                                     outs[1])
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run()
+    rng = np.random.default_rng(17)
+    for _ in range(2):
+        host = [[[torch.from_numpy(rng.uniform(-1, 1, tuple(t.shape))).to(torch.bfloat16) for t in row]
+                 for row in frame] for frame in tiles]
+        for fd, fh in zip(tiles, host):
+            for rd, rh in zip(fd, fh):
+                for td, th in zip(rd, rh):
+                    td.copy_(th)
+        for buf in [whole, band, *outs]:
+            buf.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle_stitch([[[to_storage(t, "bf16") for t in row] for row in frame] for frame in host],
+                            [lt, ly, lx], "bf16")
+        assert np.array_equal(to_storage(whole.cpu(), "bf16"), ref)
+        assert torch.equal(torch.cat(outs, dim=2).view(torch.int16), whole.view(torch.int16))
+
+
+def test_gathered_groupnorm_replays_with_new_inputs(tbl):
+    # two ranks' statistics calls writing their record sets side by side (as
+    # an all-gather lays them out) and each rank's gathered apply, in one
+    # graph; replayed with new patches, within the GroupNorm tolerance
+    from tests.tolerance import gn_violation
+    G = 8
+    shape = (1, 32, 20, 48)
+    parts = [torch.empty((1, 32, h, 48), dtype=torch.bfloat16, device="cuda") for h in (8, 12)]
+    gamma = (synth.normal_tensor(4, (32,), "bf16") * 0.1 + 1.0).cuda()
+    beta = (synth.normal_tensor(5, (32,), "bf16") * 0.1).cuda()
+    every = tbl.new_partials(2, 1, G)
+    outs = [torch.empty_like(p) for p in parts]
+
+    def run():
+        for r in range(2):
+            tbl.tb_patch_gn_stats([parts[r]], G, every[r:r + 1])
+        for r in range(2):
+            tbl.tb_patch_gn_apply_gathered([parts[r]], [outs[r]], G, every, 2, gamma, beta, 1e-6, True)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run()
+    for seed in (31, 32):
+        x = synth.normal_tensor(seed, shape, "bf16") * (1.0 + seed % 2) + (seed - 31.5)
+        cpu = [p.contiguous() for p in torch.split(x.to(torch.bfloat16), [8, 12], dim=2)]
+        for d, c in zip(parts, cpu):
+            d.copy_(c)
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        with np.errstate(over="ignore"):
+            assert gn_violation([o.cpu() for o in outs], cpu, gamma.cpu(), beta.cpu(), G, 1e-6, True, "bf16") <= 1.0
