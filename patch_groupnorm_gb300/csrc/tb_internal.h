@@ -29,6 +29,9 @@ struct StitchAxis {
 // Everything a stitch launch needs, passed by value (__grid_constant__).
 // Capacities come in two classes so that small grids launch with small
 // parameter blocks.
+// Piece ranks the one-dimensional stitch grid can index (more: two-dimensional grid).
+constexpr int STITCH_MAXR = 128;
+
 template <int MAXA, int MAXT, int MAXC>
 struct StitchParams {
     const void* tiles[MAXT];   // row-major over (k, i, j)
@@ -40,6 +43,17 @@ struct StitchParams {
     int32_t rows_per_thread;   // work per thread in a box piece (tuning)
     StitchAxis<MAXA> ax[3];    // t, y, x
     float2 coef[MAXC];         // (w, u) = ((float)(c/e), (float)(1 - c/e)) per distinct e, c < e
+    // One-dimensional grid of the pieces that exist (nrank > 0): block b is
+    // piece rank r of some (plane, tile) where rank_start[r] <= b <
+    // rank_start[r + 1]; within rank r the blocks run over planes, and within
+    // a plane over the first (rank_start[r + 1] - rank_start[r]) / planes
+    // entries of tile_order (the tiles sorted by piece count, most first, so
+    // the tiles with a piece of rank r come first).  nrank = 0: the grid is
+    // (planes x tiles, pieces of the largest tile), blocks past a tile's
+    // pieces exit at once.
+    int32_t nrank;
+    int32_t rank_start[STITCH_MAXR + 1];
+    int16_t tile_order[MAXT];
 };
 
 constexpr int SMALL_MAXA = 16, SMALL_MAXT = 256, SMALL_MAXC = 640;

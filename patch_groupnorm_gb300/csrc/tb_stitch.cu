@@ -654,13 +654,36 @@ __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_
     const auto& AY = p.ax[1];
     const auto& AX = p.ax[2];
 
-    // which tile, which box, which rows.  blockIdx.x runs over (plane, tile)
-    // with the tile fastest and blockIdx.y over the tile's pieces, heaviest
-    // first: the GPU dispatches every tile's longest pieces before any short.
+    // which tile, which box, which rows.  Pieces are ranked within their
+    // tile, heaviest first, and the blocks run rank by rank, so the GPU
+    // dispatches every tile's longest pieces before any short one.  With
+    // the one-dimensional grid (p.nrank > 0) only pieces that exist get a
+    // block: rank r holds, plane by plane, the tiles of tile_order that have
+    // more than r pieces; otherwise blockIdx.x runs over (plane, tile) with
+    // the tile fastest and blockIdx.y over the ranks.
     Piece pc;
     const int ntiles = AX.n * AY.n * (NDIM == 3 ? AT.n : 1);
-    const int tile = (int)(blockIdx.x % (unsigned)ntiles);
-    pc.plane = (int64_t)(blockIdx.x / (unsigned)ntiles);
+    int tile, piece;
+    if (p.nrank > 0) {
+        const int b = (int)blockIdx.x;
+        int lo = 0, hi = p.nrank;  // rank_start[lo] <= b < rank_start[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.rank_start[mid] <= b) lo = mid;
+            else hi = mid;
+        }
+        const unsigned idx = (unsigned)(b - p.rank_start[lo]);
+        const unsigned per_plane = (unsigned)((p.rank_start[lo + 1] - p.rank_start[lo]) / p.planes);
+        const unsigned q = idx / per_plane;
+        pc.plane = (int64_t)q;
+        tile = p.tile_order[idx - q * per_plane];
+        piece = lo;
+        if (!index_ok(tile >= 0 && tile < ntiles && pc.plane < p.planes, p.status)) return;
+    } else {
+        tile = (int)(blockIdx.x % (unsigned)ntiles);
+        pc.plane = (int64_t)(blockIdx.x / (unsigned)ntiles);
+        piece = (int)blockIdx.y;
+    }
     pc.j = tile % AX.n;
     pc.i = (tile / AX.n) % AY.n;
     pc.k = NDIM == 3 ? tile / (AX.n * AY.n) : 0;
@@ -670,7 +693,6 @@ __global__ void __launch_bounds__(STITCH_BLOCK, (NDIM == 3 ? TB_STITCH_MIN_CTAS_
     const int ebt = (NDIM == 3 && pc.k > 0) ? min(AT.blend[pc.k], Kt) : 0;
     const int eby = pc.i > 0 ? min(AY.blend[pc.i], Ky) : 0;
     const int ebx = pc.j > 0 ? min(AX.blend[pc.j], Kx) : 0;
-    int piece = blockIdx.y;
     pc.need = -1;
     constexpr int NB = NDIM == 3 ? 8 : 4;
     for (int b = NB - 1; b >= 0; --b) {  // same order as tile_pieces()
