@@ -593,11 +593,10 @@ tb_status tb_gather_patches(const void* const* patches, int32_t P, const int64_t
  *   - P * N * G * TB_GN_PARTS larger than TB_NOALLOC_MAX_PARTIALS returns
  *     TB_ERR_UNSUPPORTED and launches nothing.
  *   - The first call on each device looks up the scratch array's device
- *     address (cudaGetSymbolAddress, with that device current); make that
- *     first call before any stream capture.  The address belongs to the
- *     device's CUDA context: after cudaDeviceReset (or any other teardown of
- *     the context) the next call finds a new context id and looks the
- *     address up again, so that call, too, must come before any capture.
+ *     address (cudaGetSymbolAddress, with that device current).  The
+ *     address belongs to the device's CUDA context: after cudaDeviceReset
+ *     (or any other teardown of the context) the next call finds a new
+ *     context id and looks the address up again.
  *   - Every call uses the same scratch array.  Each call writes every record
  *     it reads before reading it, so nothing needs clearing, but two calls
  *     whose work overlaps on the GPU (different streams, or different host

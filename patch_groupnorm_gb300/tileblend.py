@@ -646,8 +646,8 @@ def tb_patch_group_norm_noalloc(patches: Sequence[torch.Tensor], outs: Sequence[
     partial statistics live in the library's own fixed scratch array (room
     for P * N * G * TB_GN_PARTS <= TB_NOALLOC_MAX_PARTIALS records), so the
     call needs no buffer besides the inputs and outputs.  Calls share that array: order
-    them on one stream.  The first call on a device looks the array up; make
-    it before any stream capture."""
+    them on one stream.  The first call on a device looks the array's
+    address up."""
     N, C, dt, spatial, ptrs = _gn_args(patches)
     P = len(patches)
     if len(outs) != P:
