@@ -283,6 +283,21 @@ def test_largest_tile_grid_bit_exact(tbl, ndim):
     _check_equal(_run_gpu(tbl, tiles, axes, "bf16", 1, 2), ref, "bf16")
 
 
+def test_tall_wide_tiles_with_more_piece_ranks_than_the_rank_table(tbl):
+    # 4096-row tiles 1536 px kept wide: a copy box one 16-byte chunk per
+    # thread across gives 16-row pieces, 192 of them for one tile -- more
+    # ranks than the one-dimensional grid's table holds -- on a grid larger
+    # than one resident wave: the two-dimensional grid is used instead
+    axes = [W.AxisSpec(512, 512, 0.25, 8), W.AxisSpec(256, 256, 0.25, 8)]
+    lays = _oracle_layouts(axes)
+    assert [l.extents for l in lays] == [[4096, 1024], [2048, 512]]
+    rng = np.random.default_rng(192)
+    tiles = [[torch.from_numpy(rng.uniform(-1, 1, (1, 3, ly, lx)).astype(np.float32)).to(torch.bfloat16)
+              for lx in lays[1].extents] for ly in lays[0].extents]
+    ref = oracle_stitch(_storage_grid(tiles, "bf16"), lays, "bf16")
+    _check_equal(_run_gpu(tbl, tiles, axes, "bf16", 1, 3), ref, "bf16")
+
+
 def test_no_kernel_reported_a_problem(tbl):
     # the device status word stays 0 through every stitch above (no copy
     # wait ran out, no bounds check fired)
