@@ -454,6 +454,7 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     l.vec = vec;
     // Pieces per tile; the grid's second extent is the largest count.
     int rpt = ndim == 3 ? TB_STITCH_ROWS_PER_THREAD_3D : TB_STITCH_ROWS_PER_THREAD;
+    std::vector<int> np(ntiles);  // pieces of tile (k, i, j), row-major, for the last count
     auto count = [&](int r, int& max_p, int64_t& total) {
         max_p = 0;
         total = 0;
@@ -463,10 +464,11 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
                     const int ebt = (ndim == 3 && k > 0) ? std::min(g[0].blend[k], g[0].kept[k]) : 0;
                     const int eby = i > 0 ? std::min(g[1].blend[i], g[1].kept[i]) : 0;
                     const int ebx = j > 0 ? std::min(g[2].blend[j], g[2].kept[j]) : 0;
-                    const int np = tb::tile_pieces(ndim, g[0].kept[k], g[1].kept[i], g[2].kept[j], ebt, eby, ebx,
-                                                   vec, r);
-                    max_p = std::max(max_p, np);
-                    total += np;
+                    const int n = tb::tile_pieces(ndim, g[0].kept[k], g[1].kept[i], g[2].kept[j], ebt, eby, ebx,
+                                                  vec, r);
+                    np[(k * g[1].n + i) * g[2].n + j] = n;
+                    max_p = std::max(max_p, n);
+                    total += n;
                 }
         total *= planes;
     };
@@ -491,10 +493,8 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
                         best_n = n;
                     }
                 }
-                if (best != rpt) {
-                    rpt = best;
-                    count(rpt, max_pieces, total_pieces);
-                }
+                rpt = best;
+                count(rpt, max_pieces, total_pieces);  // the counts (and np) of the chosen rows
             }
         }
     }
@@ -521,16 +521,6 @@ tb_status fill_and_launch(P& prm, const Axis (&g)[3], int ndim, tb_dtype dtype, 
     const bool over_a_wave = device_sms(&sms_now) == TB_OK &&
                              (int64_t)ntiles * planes * max_pieces > (int64_t)sms_now * (ndim == 3 ? 3 : 4);
     if (TB_STITCH_FLAT_GRID && over_a_wave && max_pieces <= tb::STITCH_MAXR && total_pieces <= 2147483647LL) {
-        std::vector<int> np(ntiles);
-        for (int k = 0; k < g[0].n; ++k)
-            for (int i = 0; i < g[1].n; ++i)
-                for (int j = 0; j < g[2].n; ++j) {
-                    const int ebt = (ndim == 3 && k > 0) ? std::min(g[0].blend[k], g[0].kept[k]) : 0;
-                    const int eby = i > 0 ? std::min(g[1].blend[i], g[1].kept[i]) : 0;
-                    const int ebx = j > 0 ? std::min(g[2].blend[j], g[2].kept[j]) : 0;
-                    np[(k * g[1].n + i) * g[2].n + j] =
-                        tb::tile_pieces(ndim, g[0].kept[k], g[1].kept[i], g[2].kept[j], ebt, eby, ebx, vec, rpt);
-                }
         std::vector<int> order(ntiles);
         for (int t = 0; t < ntiles; ++t) order[t] = t;
         std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return np[a] > np[b]; });
