@@ -992,7 +992,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--kernel-reps", type=int, default=30)
+    ap.add_argument("--kernel-reps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kernels", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
